@@ -1,0 +1,513 @@
+"""Pins for the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: a worked example printed on
+the pages (tests/golden/), a closed form, a special case that reduces to a library routine,
+or a second, independently written form of the same definition (step recurrence vs the
+materialised SSD matrix vs the chunked decomposition).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+from recurrent_state_update_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = (s.strip() for s in line.split("=", 1))
+                out[k] = v
+    return out
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------------------------
+# the affine-transition example printed on the page
+# ----------------------------------------------------------------------------------------
+
+def _scalar_inputs(a_seq, b_seq):
+    """Scalar SSM (H=P=N=G=1, A=-1, no softplus, B=C=1, D=0) whose token t applies
+    h <- a_t h + b_t:  Delta_t = -ln a_t makes exp(Delta_t A) = a_t, and x_t = b_t / Delta_t
+    makes Delta_t B x_t = b_t.  y_t = C h_t = h_t."""
+    a_seq = np.asarray(a_seq, float)
+    b_seq = np.asarray(b_seq, float)
+    delta = -np.log(a_seq)
+    T = len(a_seq)
+    x = (b_seq / delta).reshape(T, 1, 1)
+    ones = np.ones((T, 1, 1))
+    return dict(x=x, dt=delta.reshape(T, 1), A=np.array([-1.0]), B=ones, C=ones)
+
+
+def _compose(first, second):
+    # the page's composition rule: (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2)
+    a1, b1 = first
+    a2, b2 = second
+    return a2 * a1, a2 * b1 + b2
+
+
+def test_affine_composition_page_example():
+    g = _golden("affine_scan.txt")
+    steps = [tuple(float(v) for v in s.split(",")) for s in g["steps"].split()]
+    left = _compose(_compose(steps[0], steps[1]), steps[2])
+    right = _compose(steps[0], _compose(steps[1], steps[2]))
+    np.testing.assert_allclose(left, right, rtol=1e-15)
+    inp = _scalar_inputs([s[0] for s in steps], [s[1] for s in steps])
+    for h0 in (0.0, 1.5, -3.0):
+        expect = left[0] * h0 + left[1]
+        # decode path, token by token
+        h, y = oracle.ssm_update(np.full((1, 1, 1), h0), inp["x"], inp["B"], inp["C"], inp["dt"],
+                                 inp["A"], dt_softplus=False)
+        assert h[0, 0, 0] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+        assert y[-1, 0, 0] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+        # prefill by steps, materialised and chunked (every chunk length)
+        cu = np.array([0, 3], np.int32)
+        _, hf, _ = oracle.prefill_steps(cu, inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                        h0=np.full((1, 1, 1, 1), h0), dt_softplus=False)
+        assert hf[0, 0, 0, 0] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+        _, hm = oracle.prefill_materialised(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                            h0=np.full((1, 1, 1), h0), dt_softplus=False)
+        assert hm[0, 0, 0] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+        for q in (1, 2, 3):
+            _, hc = oracle.prefill_chunked(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], chunk=q,
+                                           h0=np.full((1, 1, 1), h0), dt_softplus=False)
+            assert hc[0, 0, 0] == pytest.approx(expect, rel=1e-13, abs=1e-13)
+
+
+@pytest.mark.parametrize("factor", [0.9, 1.1])
+def test_restored_error_propagates_by_factor_power(factor):
+    g = _golden("affine_scan.txt")
+    n = int(g["nsteps"])
+    inc = float(g["increment"])
+    e0, r0 = float(g["exact_start"]), float(g["restored_start"])
+    # factor 1.1 > 1 is an "amplifying" step: exp(Delta*A) = 1.1 needs Delta*A > 0, which the
+    # scalar system gets from A = +1 and Delta = ln 1.1 (no softplus, so Delta is used as given).
+    delta = abs(math.log(factor))
+    A = np.array([math.copysign(1.0, math.log(factor))])
+    x = np.full((n, 1, 1), inc / delta)
+    ones = np.ones((n, 1, 1))
+    dt = np.full((n, 1), delta)
+    he, ye = oracle.ssm_update(np.full((1, 1, 1), e0), x, ones, ones, dt, A, dt_softplus=False)
+    hr, yr = oracle.ssm_update(np.full((1, 1, 1), r0), x, ones, ones, dt, A, dt_softplus=False)
+    assert hr[0, 0, 0] - he[0, 0, 0] == pytest.approx((r0 - e0) * factor ** n, rel=1e-9)
+    # the page's own loop for the exact trajectory
+    exact = e0
+    for _ in range(n):
+        exact = factor * exact + inc
+    assert he[0, 0, 0] == pytest.approx(exact, rel=1e-12)
+
+
+# ----------------------------------------------------------------------------------------
+# closed forms
+# ----------------------------------------------------------------------------------------
+
+def _random_problem(seed, H=4, P=3, N=5, G=2, T=7):
+    g = _rng(seed)
+    return dict(
+        h0=0.3 * g.standard_normal((H, P, N)),
+        x=g.standard_normal((T, H, P)),
+        B=g.standard_normal((T, G, N)),
+        C=g.standard_normal((T, G, N)),
+        dt=g.uniform(-5, 0, size=(T, H)),
+        A=-np.exp(g.uniform(0, np.log(16), size=H)),
+        D=g.standard_normal(H),
+        dt_bias=g.uniform(-2, 1, size=H),
+        z=g.standard_normal((T, H, P)),
+    )
+
+
+def _group(h, H, G):
+    return h // (H // G)
+
+
+def _run_decode_path(pr, h0, **kw):
+    return oracle.ssm_update(h0, pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"], **kw)
+
+
+def _run_prefill_path(pr, h0, **kw):
+    T = pr["x"].shape[0]
+    y, hf, _ = oracle.prefill_steps(np.array([0, T], np.int32), pr["x"], pr["dt"], pr["A"], pr["B"],
+                                    pr["C"], h0=h0[None], **kw)
+    return hf[0], y
+
+
+@pytest.mark.parametrize("path", [_run_decode_path, _run_prefill_path])
+def test_constant_inputs_geometric_series(path):
+    """Constant x, B, C, dt: h_T = a^T h0 + (1 - a^T)/(1 - a) * Delta x B^T per head."""
+    pr = _random_problem(1)
+    T, H, P = pr["x"].shape
+    G, N = pr["B"].shape[1:]
+    for k in ("x", "B", "C", "dt"):
+        pr[k] = np.repeat(pr[k][:1], T, axis=0)
+    h, y = path(pr, pr["h0"], D=pr["D"], dt_bias=pr["dt_bias"], dt_softplus=True)
+    s = pr["dt"][0] + pr["dt_bias"]
+    delta = np.logaddexp(0.0, s)  # softplus via the library routine
+    for hh in range(H):
+        gg = _group(hh, H, G)
+        a = math.exp(delta[hh] * pr["A"][hh])
+        inj = delta[hh] * np.outer(pr["x"][0, hh], pr["B"][0, gg])
+        expect = a ** T * pr["h0"][hh] + (1 - a ** T) / (1 - a) * inj
+        np.testing.assert_allclose(h[hh], expect, rtol=1e-11, atol=1e-13)
+        y_expect = expect @ pr["C"][0, gg] + pr["D"][hh] * pr["x"][0, hh]
+        np.testing.assert_allclose(y[-1, hh], y_expect, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("path", [_run_decode_path, _run_prefill_path])
+def test_zero_A_is_a_prefix_sum(path):
+    """A = 0 makes exp(Delta A) = 1: h_T = h0 + sum_t Delta_t x_t B_t^T."""
+    pr = _random_problem(2)
+    T, H, P = pr["x"].shape
+    G = pr["B"].shape[1]
+    pr["A"] = np.zeros(H)
+    h, y = path(pr, pr["h0"], dt_bias=pr["dt_bias"], dt_softplus=True)
+    delta = np.logaddexp(0.0, pr["dt"] + pr["dt_bias"])
+    for hh in range(H):
+        gg = _group(hh, H, G)
+        expect = pr["h0"][hh] + np.einsum("t,tp,tn->pn", delta[:, hh], pr["x"][:, hh], pr["B"][:, gg])
+        np.testing.assert_allclose(h[hh], expect, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("path", [_run_decode_path, _run_prefill_path])
+def test_delta_to_zero_leaves_state(path):
+    """dt_bias -> -inf drives Delta -> 0: h unchanged, y = C.h + D*x."""
+    pr = _random_problem(3)
+    T, H, P = pr["x"].shape
+    G = pr["B"].shape[1]
+    bias = np.full(H, -80.0)
+    h, y = path(pr, pr["h0"], D=pr["D"], dt_bias=bias, dt_softplus=True)
+    np.testing.assert_allclose(h, pr["h0"], rtol=1e-20, atol=1e-30)
+    for hh in range(H):
+        gg = _group(hh, H, G)
+        y_expect = pr["h0"][hh] @ pr["C"][:, gg].T + pr["D"][hh] * pr["x"][:, hh].T  # (P, T)
+        np.testing.assert_allclose(y[:, hh].T, y_expect, rtol=1e-13, atol=1e-14)
+
+
+def test_softplus_matches_library():
+    """Scalar: A = 0, h0 = 0, B = x = 1: after one token h = Delta = softplus(dt + bias)."""
+    for s in (-700.0, -40.0, -5.0, -1e-3, 0.0, 1e-3, 3.0, 40.0, 700.0):
+        h, _ = oracle.ssm_update(np.zeros((1, 1, 1)), np.ones((1, 1, 1)), np.ones((1, 1, 1)),
+                                 np.ones((1, 1, 1)), np.array([[s]]), np.zeros(1),
+                                 dt_bias=np.array([0.0]), dt_softplus=True)
+        assert h[0, 0, 0] == pytest.approx(np.logaddexp(0.0, s), rel=1e-15, abs=1e-300)
+
+
+def test_gate_is_silu_of_z():
+    """y with z equals y without z times z*sigmoid(z) (sigmoid from scipy)."""
+    pr = _random_problem(4)
+    _, y0 = _run_decode_path(pr, pr["h0"], D=pr["D"], dt_bias=pr["dt_bias"])
+    _, y1 = _run_decode_path(pr, pr["h0"], D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    np.testing.assert_allclose(y1, y0 * pr["z"] * expit(pr["z"]), rtol=1e-14, atol=1e-15)
+
+
+def test_D_skip_term():
+    """D enters as y += D*x: the difference of runs with and without D is D*x exactly."""
+    pr = _random_problem(5)
+    _, y0 = _run_decode_path(pr, pr["h0"], dt_bias=pr["dt_bias"])
+    _, y1 = _run_decode_path(pr, pr["h0"], D=pr["D"], dt_bias=pr["dt_bias"])
+    np.testing.assert_allclose(y1 - y0, pr["D"][None, :, None] * pr["x"], rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------------------
+# conv1d
+# ----------------------------------------------------------------------------------------
+
+def test_conv_identity_tap_is_silu_and_shift():
+    g = _rng(6)
+    Cd, W, Wc, T = 6, 4, 3, 5
+    st = g.standard_normal((Cd, Wc))
+    u = g.standard_normal((T, Cd))
+    w = np.zeros((Cd, W))
+    w[:, W - 1] = 1.0
+    st2, out = oracle.conv_update(st, u, w)
+    np.testing.assert_allclose(out, u * expit(u), rtol=1e-15)
+    np.testing.assert_array_equal(st2, u[-Wc:].T)
+
+
+@pytest.mark.parametrize("Wc,ntok", [(3, 1), (3, 9), (7, 4), (7, 1)])
+def test_conv_matches_numpy_convolve(Wc, ntok):
+    """Causal conv of the full input history (np.convolve) + bias, then SiLU."""
+    g = _rng(7 + Wc + ntok)
+    Cd, W = 5, 4
+    st = g.standard_normal((Cd, Wc))
+    u = g.standard_normal((ntok, Cd))
+    w = g.standard_normal((Cd, W))
+    b = g.standard_normal(Cd)
+    st2, out = oracle.conv_update(st, u, w, b)
+    for c in range(Cd):
+        hist = np.concatenate([st[c], u[:, c]])
+        full = np.convolve(hist, w[c, ::-1])  # full[m] = sum_k hist[m-W+1+k] * w[k]
+        v = full[Wc: Wc + ntok] + b[c]
+        np.testing.assert_allclose(out[:, c], v * expit(v), rtol=1e-13, atol=1e-14)
+        np.testing.assert_array_equal(st2[c], hist[-Wc:])
+    # one token per call gives the same as all tokens in one call
+    s = st.copy()
+    outs = []
+    for j in range(ntok):
+        s, o = oracle.conv_update(s, u[j:j + 1], w, b)
+        outs.append(o)
+    np.testing.assert_allclose(np.concatenate(outs), out, rtol=1e-15)
+    np.testing.assert_array_equal(s, st2)
+
+
+# ----------------------------------------------------------------------------------------
+# the SSD identity and the chunk decomposition
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,G,with_h0,with_z", [(1, 1, False, False), (17, 1, True, False),
+                                                (40, 2, True, True), (64, 2, False, True)])
+def test_step_recurrence_equals_materialised_ssd(T, G, with_h0, with_z):
+    pr = _random_problem(10 + T, H=2 * G, P=4, N=4, G=G, T=T)
+    h0 = pr["h0"] if with_h0 else None
+    z = pr["z"] if with_z else None
+    y_s, hf_s, _ = oracle.prefill_steps(np.array([0, T], np.int32), pr["x"], pr["dt"], pr["A"], pr["B"],
+                                        pr["C"], h0=None if h0 is None else h0[None], D=pr["D"],
+                                        dt_bias=pr["dt_bias"], z=z)
+    y_m, hf_m = oracle.prefill_materialised(pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], h0=h0,
+                                            D=pr["D"], dt_bias=pr["dt_bias"], z=z)
+    np.testing.assert_allclose(y_m, y_s, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hf_m, hf_s[0], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("Q", [1, 64, 256, 700, 1024])
+def test_chunked_equals_step_recurrence(Q):
+    T = 700  # with Q=256: two full chunks and a partial one
+    pr = _random_problem(20, H=4, P=4, N=8, G=2, T=T)
+    y_s, hf_s, _ = oracle.prefill_steps(np.array([0, T], np.int32), pr["x"], pr["dt"], pr["A"], pr["B"],
+                                        pr["C"], h0=pr["h0"][None], D=pr["D"], dt_bias=pr["dt_bias"],
+                                        z=pr["z"])
+    y_c, hf_c = oracle.prefill_chunked(pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], chunk=Q,
+                                       h0=pr["h0"], D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    np.testing.assert_allclose(y_c, y_s, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hf_c, hf_s[0], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_steps_equal_prefill():
+    """T single-token decode steps reproduce the prefill of the same T tokens."""
+    pr = _random_problem(30, T=9)
+    h = pr["h0"].copy()
+    ys = []
+    for t in range(9):
+        h, y = oracle.ssm_update(h, pr["x"][t:t + 1], pr["B"][t:t + 1], pr["C"][t:t + 1],
+                                 pr["dt"][t:t + 1], pr["A"], D=pr["D"], dt_bias=pr["dt_bias"],
+                                 z=pr["z"][t:t + 1])
+        ys.append(y[0])
+    y_p, hf, _ = oracle.prefill_steps(np.array([0, 9], np.int32), pr["x"], pr["dt"], pr["A"], pr["B"],
+                                      pr["C"], h0=pr["h0"][None], D=pr["D"], dt_bias=pr["dt_bias"],
+                                      z=pr["z"])
+    np.testing.assert_allclose(np.stack(ys), y_p, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(h, hf[0], rtol=1e-14, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------------------
+# varlen prefill, hand-off and checkpoints
+# ----------------------------------------------------------------------------------------
+
+def _varlen_problem(seed, lengths, H=4, P=3, N=4, G=2):
+    T = int(sum(lengths))
+    pr = _random_problem(seed, H=H, P=P, N=N, G=G, T=T)
+    pr["cu"] = wl.cu_seqlens(lengths)
+    pr["h0s"] = 0.3 * _rng(seed + 1).standard_normal((len(lengths), H, P, N))
+    return pr
+
+
+def test_varlen_sequences_are_independent():
+    lengths = [5, 1, 12, 7]
+    pr = _varlen_problem(40, lengths)
+    y, hf, _ = oracle.prefill_steps(pr["cu"], pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], h0=pr["h0s"],
+                                    D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    for s, (a, b) in enumerate(zip(pr["cu"][:-1], pr["cu"][1:])):
+        ym, hm = oracle.prefill_materialised(pr["x"][a:b], pr["dt"][a:b], pr["A"], pr["B"][a:b],
+                                             pr["C"][a:b], h0=pr["h0s"][s], D=pr["D"],
+                                             dt_bias=pr["dt_bias"], z=pr["z"][a:b])
+        np.testing.assert_allclose(y[a:b], ym, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(hf[s], hm, rtol=1e-12, atol=1e-12)
+
+
+def test_chunked_prefill_handoff_equals_one_pass():
+    """Seeding the second part from the first part's final state equals one pass (state hand-off)."""
+    pr = _varlen_problem(50, [23])
+    T = 23
+    y, hf, _ = oracle.prefill_steps(pr["cu"], pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], h0=pr["h0s"],
+                                    D=pr["D"], dt_bias=pr["dt_bias"])
+    cut = 10
+    sl = lambda a, b: dict(x=pr["x"][a:b], dt=pr["dt"][a:b], B=pr["B"][a:b], C=pr["C"][a:b])
+    p1, p2 = sl(0, cut), sl(cut, T)
+    y1, h1, _ = oracle.prefill_steps(np.array([0, cut], np.int32), p1["x"], p1["dt"], pr["A"], p1["B"],
+                                     p1["C"], h0=pr["h0s"], D=pr["D"], dt_bias=pr["dt_bias"])
+    y2, h2, _ = oracle.prefill_steps(np.array([0, T - cut], np.int32), p2["x"], p2["dt"], pr["A"],
+                                     p2["B"], p2["C"], h0=h1, D=pr["D"], dt_bias=pr["dt_bias"])
+    np.testing.assert_allclose(np.concatenate([y1, y2]), y, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(h2, hf, rtol=1e-13, atol=1e-14)
+
+
+def test_checkpoints_are_prefix_final_states():
+    lengths = [9, 4, 13]
+    interval, max_ckpt = 4, 3
+    pr = _varlen_problem(60, lengths)
+    _, hf, hc = oracle.prefill_steps(pr["cu"], pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], h0=pr["h0s"],
+                                     dt_bias=pr["dt_bias"], ckpt_interval=interval, max_ckpt=max_ckpt)
+    for s, L in enumerate(lengths):
+        a = pr["cu"][s]
+        for k in range(1, max_ckpt + 1):
+            if k * interval <= L:
+                b = a + k * interval
+                _, hm = oracle.prefill_materialised(pr["x"][a:b], pr["dt"][a:b], pr["A"], pr["B"][a:b],
+                                                    pr["C"][a:b], h0=pr["h0s"][s], dt_bias=pr["dt_bias"])
+                np.testing.assert_allclose(hc[s, k - 1], hm, rtol=1e-12, atol=1e-12)
+            else:
+                assert np.isnan(hc[s, k - 1]).all()
+    # a length that is a multiple of the interval: the last checkpoint is the final state
+    np.testing.assert_allclose(hc[1, 0], hf[1], rtol=0, atol=0)
+
+
+# ----------------------------------------------------------------------------------------
+# the slot pool: gather by slot id, padding, scratch slots, speculative commit
+# ----------------------------------------------------------------------------------------
+
+def _pool_problem(seed, shape, S, batch, ntok, pad=0):
+    g = _rng(seed)
+    H, P, N, G = shape.nheads, shape.head_dim, shape.d_state, shape.n_groups
+    Cd, Wc = shape.conv_dim, shape.conv_cols
+    slot = g.choice(S, size=batch, replace=False).astype(np.int32)
+    if pad:
+        slot[g.choice(batch, size=pad, replace=False)] = -1
+    return dict(
+        ssm=0.1 * g.standard_normal((S, H, P, N)),
+        conv=0.1 * g.standard_normal((S, Cd, Wc)),
+        conv_w=g.standard_normal((Cd, shape.conv_kernel)) / 2,
+        slot=slot,
+        xbc=g.standard_normal((batch, ntok, Cd)),
+        dt=g.uniform(-6, -3, size=(batch, ntok, H)),
+        A=-np.exp(g.uniform(0, np.log(16), size=H)),
+        D=g.standard_normal(H),
+        dt_bias=g.uniform(-1, 1, size=H),
+        z=g.standard_normal((batch, ntok, H, P)),
+    )
+
+
+SMALL = wl.LayerShape(nheads=4, head_dim=3, d_state=4, n_groups=2, conv_kernel=4)
+
+
+def test_decode_pool_matches_per_request_functions_and_skips_padding():
+    S, batch, ntok = 9, 6, 2
+    pr = _pool_problem(70, SMALL, S, batch, ntok, pad=2)
+    ssm, conv = pr["ssm"].copy(), pr["conv"].copy()
+    y = oracle.decode(ssm, pr["slot"], pr["xbc"], pr["dt"], pr["A"], conv_pool=conv, conv_w=pr["conv_w"],
+                      D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"], n_groups=SMALL.n_groups)
+    HP, GN = SMALL.nheads * SMALL.head_dim, SMALL.n_groups * SMALL.d_state
+    touched = set()
+    for i, s in enumerate(pr["slot"]):
+        if s < 0:
+            assert np.isnan(y[i]).all()
+            continue
+        touched.add(int(s))
+        st, post = oracle.conv_update(pr["conv"][s], pr["xbc"][i], pr["conv_w"])
+        np.testing.assert_array_equal(conv[s], st)
+        x = post[:, :HP].reshape(ntok, SMALL.nheads, SMALL.head_dim)
+        B = post[:, HP:HP + GN].reshape(ntok, SMALL.n_groups, SMALL.d_state)
+        C = post[:, HP + GN:].reshape(ntok, SMALL.n_groups, SMALL.d_state)
+        h, yy = oracle.ssm_update(pr["ssm"][s], x, B, C, pr["dt"][i], pr["A"], D=pr["D"],
+                                  dt_bias=pr["dt_bias"], z=pr["z"][i])
+        np.testing.assert_array_equal(ssm[s], h)
+        np.testing.assert_array_equal(y[i], yy)
+    for s in range(S):
+        if s not in touched:
+            np.testing.assert_array_equal(ssm[s], pr["ssm"][s])
+            np.testing.assert_array_equal(conv[s], pr["conv"][s])
+
+
+def test_decode_permuted_slots_permute_results():
+    S, batch = 8, 5
+    pr = _pool_problem(80, SMALL, S, batch, 1)
+    perm = _rng(81).permutation(batch)
+    ssm1, conv1 = pr["ssm"].copy(), pr["conv"].copy()
+    y1 = oracle.decode(ssm1, pr["slot"], pr["xbc"], pr["dt"], pr["A"], conv_pool=conv1, conv_w=pr["conv_w"],
+                       D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"], n_groups=2)
+    ssm2, conv2 = pr["ssm"].copy(), pr["conv"].copy()
+    y2 = oracle.decode(ssm2, pr["slot"][perm], pr["xbc"][perm], pr["dt"][perm], pr["A"], conv_pool=conv2,
+                       conv_w=pr["conv_w"], D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"][perm], n_groups=2)
+    np.testing.assert_array_equal(y2, y1[perm])
+    np.testing.assert_array_equal(ssm2, ssm1)
+    np.testing.assert_array_equal(conv2, conv1)
+
+
+def test_speculative_scratch_states_and_commit():
+    """Scratch slot j holds the state after j+1 sequential decode steps; the commit of a accepted
+    tokens leaves slot and conv window as a sequential decode of exactly a tokens would."""
+    shape = SMALL.with_spec(4)
+    K = 4
+    S, batch = 24, 4
+    pr = _pool_problem(90, shape, S, batch, K)
+    g = _rng(91)
+    free = np.setdiff1d(np.arange(S), pr["slot"])
+    scratch = g.choice(free, size=(batch, K), replace=False).astype(np.int32)
+    ssm, conv = pr["ssm"].copy(), pr["conv"].copy()
+    kw = dict(D=pr["D"], dt_bias=pr["dt_bias"], n_groups=2)
+    y = oracle.decode(ssm, pr["slot"], pr["xbc"], pr["dt"], pr["A"], conv_pool=conv, conv_w=pr["conv_w"],
+                      scratch=scratch, z=pr["z"], **kw)
+    np.testing.assert_array_equal(ssm[pr["slot"]], pr["ssm"][pr["slot"]])  # main slots unchanged
+    # reference: one token at a time, in place
+    ref_ssm, ref_conv = pr["ssm"].copy(), pr["conv"].copy()
+    seq_states, seq_convs = [], []
+    for j in range(K):
+        yj = oracle.decode(ref_ssm, pr["slot"], pr["xbc"][:, j:j + 1], pr["dt"][:, j:j + 1], pr["A"],
+                           conv_pool=ref_conv, conv_w=pr["conv_w"], z=pr["z"][:, j:j + 1], **kw)
+        np.testing.assert_allclose(y[:, j], yj[:, 0], rtol=1e-14, atol=1e-15)
+        seq_states.append(ref_ssm[pr["slot"]].copy())
+        seq_convs.append(ref_conv[pr["slot"]].copy())
+        np.testing.assert_allclose(ssm[scratch[:, j]], seq_states[j], rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(conv[pr["slot"]], seq_convs[-1])
+    accept = np.array([0, 1, 3, 4], np.int32)
+    oracle.spec_commit(ssm, pr["slot"], scratch, accept, conv_pool=conv)
+    W1 = shape.conv_kernel - 1
+    for i, (s, a) in enumerate(zip(pr["slot"], accept)):
+        if a == 0:
+            np.testing.assert_array_equal(ssm[s], pr["ssm"][s])
+            np.testing.assert_array_equal(conv[s][:, -W1:], pr["conv"][s][:, -W1:])
+        else:
+            np.testing.assert_allclose(ssm[s], seq_states[a - 1][i], rtol=1e-14, atol=1e-15)
+            np.testing.assert_array_equal(conv[s][:, -W1:], seq_convs[a - 1][i][:, -W1:])
+        # the freed columns on the left are zero
+        np.testing.assert_array_equal(conv[s][:, :K - a], 0.0)
+
+
+# ----------------------------------------------------------------------------------------
+# the input recipe's storage rounding
+# ----------------------------------------------------------------------------------------
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    g = _rng(100)
+    v = np.concatenate([g.standard_normal(10000) * 10.0 ** g.integers(-30, 30, 10000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.0e38, -1e-40]]).astype(np.float32)
+    ours = wl.f32_to_bf16_bits(v)
+    theirs = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, theirs)
+    np.testing.assert_array_equal(wl.bf16_bits_to_f32(ours), torch.from_numpy(v).to(torch.bfloat16).float().numpy())
+
+
+def test_input_recipe_ranges():
+    g = wl.rng(1, 0, 0)
+    shape = wl.NEMOTRON_H_8B
+    prm = wl.layer_params(g, shape)
+    assert (prm["A"] <= -1.0).all() and (prm["A"] >= -16.0).all()
+    inp = wl.decode_inputs(g, shape, prm, 64, 1, wl.BF16)
+    delta = np.logaddexp(0.0, inp["dt"].astype(np.float64) + prm["dt_bias"])
+    assert delta.min() >= 1e-3 * (1 - 1e-6) and delta.max() <= 0.1 * (1 + 1e-6)
+    lens = wl.prefill_lengths(wl.rng(3), 8, 512, 8192, 32768)
+    assert lens.sum() == 32768 and lens.min() >= 512 and lens.max() <= 8192
+    ids = wl.slot_ids(g, 1536, 1024, 0.1)
+    assert (ids == -1).sum() == round(0.1 * 1024)
+    live = ids[ids >= 0]
+    assert len(np.unique(live)) == len(live)
