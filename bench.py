@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba2 recurrent-state update on GB300.
+
+One step = one Nemotron-H-8B-shaped decode token through all 48 Mamba2 layers for a batch of
+256 requests drawn (random, non-contiguous) from a 512-slot pool per layer: per layer one
+fused launch (conv shift + conv1d + SiLU, softplus step, state update, C.h + D.x, SiLU(z) gate)
+reading and writing each request's 2 MiB bf16 state in place.  The chunked prefill (8 varlen
+sequences of 512..8192 tokens summing to 32768, chunk 256, checkpoints every 1024 tokens) is
+timed after it and reported in the same line.
+
+Metric: decode state-update GB/s (algorithmic bytes / time) and token-layers/s against HBM
+peak; prefill tokens/s.  Inputs are synthetic and seeded (no dataset): the value distributions
+are the ones in recurrent_state_update_gb300.workloads.  The state pool of one layer
+(512 MiB touched per launch) is larger than L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from recurrent_state_update_gb300 import workloads as wl  # noqa: E402
+
+DECODE = wl.NEMOTRON_DECODE
+PREFILL = wl.CHUNKED_PREFILL
+SHAPE = wl.NEMOTRON_H_8B
+H, P, N, G = SHAPE.nheads, SHAPE.head_dim, SHAPE.d_state, SHAPE.n_groups
+CD = SHAPE.conv_dim
+W1 = SHAPE.conv_kernel - 1
+
+# Algorithmic bytes of one decode token-layer (bf16 state and activations, fp32 dt):
+#   state read + write 2*H*P*N*2, conv state read + write 2*CD*(W-1)*2, xBC in CD*2,
+#   z in H*P*2, dt in H*4, y out H*P*2.  Per-launch constants (conv taps, A, D, dt_bias) excluded.
+DECODE_BYTES_PER_TOKEN_LAYER = 2 * H * P * N * 2 + 2 * CD * W1 * 2 + CD * 2 + H * P * 2 + H * 4 + H * P * 2
+
+
+def prefill_bytes(T: int, nseq: int, n_state_writes: int) -> int:
+    """Algorithmic bytes of one prefill launch: x, B, C, dt in, y out, state writes (bf16)."""
+    return T * H * P * 2 + 2 * T * G * N * 2 + T * H * 4 + T * H * P * 2 + n_state_writes * H * P * N * 2
+
+
+def prefill_flops(lengths, chunk: int) -> float:
+    """Algorithmic flops of the chunked form (causal halves of the intra-chunk matmuls counted):
+    per chunk of length L and group: C B^T L(L+1)/2 * 2N; per head: masked (G . L) X L(L+1)/2 * 2P,
+    chunk state 2 L P N, off-diagonal C h 2 L N P."""
+    total = 0.0
+    for Ls in lengths:
+        for c0 in range(0, int(Ls), chunk):
+            L = min(chunk, int(Ls) - c0)
+            tri = L * (L + 1) / 2
+            total += G * tri * 2 * N + H * (tri * 2 * P + 2 * L * P * N + 2 * L * N * P)
+    return total
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _profile_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when the summary
+    is missing or was taken on a different version of the kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    src = vals.get("source")
+    if not src or "traffic_bytes_per_launch" not in vals:
+        return None
+    try:
+        digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if digest != vals.get("source_sha256_16"):
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+
+class DecodeWorkload:
+    """48 layers of pools, parameters and one step's inputs, resident on the device."""
+
+    def __init__(self, torch, rank: int, layers: int, batch: int, pool: int):
+        from recurrent_state_update_gb300 import binding as bd
+        self.torch, self.bd = torch, bd
+        self.layers, self.batch, self.pool = layers, batch, pool
+        self.desc = bd.layer_desc(SHAPE, state=wl.BF16, act=wl.BF16, dt=wl.F32)
+        dev = torch.device("cuda")
+        seed = DECODE["seed"] * 1000 + rank
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        bf = torch.bfloat16
+        # slot pools [layer, slot, ...], N(0, 0.1^2), generated on the device
+        self.ssm = torch.empty(layers, pool, H, P, N, dtype=bf, device=dev)
+        self.conv = torch.empty(layers, pool, CD, W1, dtype=bf, device=dev)
+        for l in range(layers):
+            self.ssm[l].copy_(torch.randn(pool, H, P, N, generator=gen, device=dev).mul_(0.1))
+            self.conv[l].copy_(torch.randn(pool, CD, W1, generator=gen, device=dev).mul_(0.1))
+        self.prm, self.slot, self.inp, self.host_inp = [], [], [], []
+        for l in range(layers):
+            g = wl.rng(seed, l)
+            prm = wl.layer_params(g, SHAPE)
+            self.prm.append({k: torch.from_numpy(v).to(dev) for k, v in prm.items()})
+            ids = wl.slot_ids(g, pool, batch)
+            self.slot.append(torch.from_numpy(ids).to(dev))
+            inp = wl.decode_inputs(g, SHAPE, prm, batch, 1, wl.BF16)
+            host = {
+                "xbc": torch.from_numpy(inp["xbc"].view(np.int16)).view(bf).pin_memory(),
+                "dt": torch.from_numpy(inp["dt"]).pin_memory(),
+                "z": torch.from_numpy(inp["z"].view(np.int16)).view(bf).pin_memory(),
+                "slot": torch.from_numpy(ids).pin_memory(),
+            }
+            self.host_inp.append(host)
+            self.inp.append({k: v.to(dev) for k, v in host.items() if k != "slot"})
+        self.y = torch.empty(layers, batch, 1, H * P, dtype=bf, device=dev)
+        self.y_host = torch.empty(layers, batch, 1, H * P, dtype=bf).pin_memory()
+        self.launches_per_step = layers
+
+    def step(self, stream=None):
+        bd = self.bd
+        for l in range(self.layers):
+            inp, prm = self.inp[l], self.prm[l]
+            bd.mamba_state_update(self.desc, self.ssm[l], self.slot[l], inp["xbc"], inp["dt"], prm["A"], self.y[l],
+                                  conv_pool=self.conv[l], conv_w=prm["conv_w"], D=prm["D"],
+                                  dt_bias=prm["dt_bias"], z=inp["z"], stream=stream)
+
+    def step_e2e(self):
+        """Host buffers in, result out: H2D copies of every layer's inputs from pinned memory,
+        the 48 launches, and the D2H copy of every layer's y."""
+        for l in range(self.layers):
+            h, d = self.host_inp[l], self.inp[l]
+            for k in ("xbc", "dt", "z"):
+                d[k].copy_(h[k], non_blocking=True)
+            self.slot[l].copy_(h["slot"], non_blocking=True)
+        self.step()
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for h in self.host_inp for t in h.values())
+
+    def d2h_bytes(self):
+        return self.y_host.numel() * self.y_host.element_size()
+
+    def bytes_per_step(self):
+        return self.layers * self.batch * DECODE_BYTES_PER_TOKEN_LAYER
+
+
+class PrefillWorkload:
+    """One layer of the varlen chunked prefill, inputs resident on the device."""
+
+    def __init__(self, torch, rank: int):
+        from recurrent_state_update_gb300 import binding as bd
+        self.torch, self.bd = torch, bd
+        dev = torch.device("cuda")
+        seed = PREFILL["seed"] * 1000 + rank
+        g = wl.rng(seed, 0)
+        self.lengths = wl.prefill_lengths(g, PREFILL["nseq"], PREFILL["len_lo"], PREFILL["len_hi"], PREFILL["total"])
+        T = int(self.lengths.sum())
+        self.T = T
+        cu = wl.cu_seqlens(self.lengths)
+        prm = wl.layer_params(g, SHAPE)
+        inp = wl.prefill_inputs(g, SHAPE, prm, T, wl.BF16)
+        bf = torch.bfloat16
+        self.desc = bd.layer_desc(SHAPE, state=wl.BF16, act=wl.BF16, dt=wl.F32)
+        nseq = len(self.lengths)
+        interval = PREFILL["ckpt_interval"]
+        max_ckpt = int(self.lengths.max()) // interval
+        n_ckpt = int(sum(int(L) // interval for L in self.lengths))
+        S = nseq + nseq * max_ckpt
+        self.pool = torch.zeros(S, H, P, N, dtype=bf, device=dev)
+        self.slot = torch.arange(nseq, dtype=torch.int32, device=dev)
+        ck = np.arange(nseq, nseq + nseq * max_ckpt, dtype=np.int32).reshape(nseq, max_ckpt)
+        self.ckpt = torch.from_numpy(ck).to(dev)
+        self.cu = torch.from_numpy(cu).to(dev)
+        self.prm = {k: torch.from_numpy(v).to(dev) for k, v in prm.items()}
+        self.x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(bf)
+        self.B = torch.from_numpy(inp["B"].view(np.int16)).to(dev).view(bf)
+        self.C = torch.from_numpy(inp["C"].view(np.int16)).to(dev).view(bf)
+        self.dt = torch.from_numpy(inp["dt"]).to(dev)
+        self.y = torch.empty_like(self.x)
+        wsb = bd.mamba_chunk_scan_workspace_bytes(self.desc, T, nseq, PREFILL["chunk"])
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        self.interval = interval
+        self.n_state_writes = nseq + n_ckpt
+
+    def step(self):
+        self.bd.mamba_chunk_scan(self.desc, self.pool, self.cu, self.slot, self.x, self.dt, self.prm["A"], self.B,
+                                 self.C, self.y, self.ws, ckpt_slots=self.ckpt, ckpt_interval=self.interval,
+                                 chunk=PREFILL["chunk"], D=self.prm["D"], dt_bias=self.prm["dt_bias"])
+
+
+def _time(torch, fn, steps, warmup, dist=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def _max_over_ranks(torch, dist, v):
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline_decode(budget_s: float = 10.0, rows: int = 32):
+    """The fp64 oracle (as it stands) on a bounded sample of the decode workload: `rows` rows of
+    one layer's batch, repeated until about `budget_s` seconds of CPU time have passed."""
+    import oracle
+    seed = DECODE["seed"] * 1000
+    g = wl.rng(seed, 0)
+    prm = wl.layer_params(g, SHAPE)
+    inp = wl.decode_inputs(g, SHAPE, prm, rows, 1, wl.BF16)
+    st = wl.initial_states(wl.rng(seed, 99), SHAPE, rows, wl.BF16, wl.BF16)
+    ssm = wl.upcast(st["ssm"], wl.BF16)
+    conv = wl.upcast(st["conv"], wl.BF16)
+    xbc = wl.upcast(inp["xbc"], wl.BF16)
+    z = wl.upcast(inp["z"], wl.BF16).reshape(rows, 1, H, P)
+    dt = inp["dt"].astype(np.float64)
+    o = {k: v.astype(np.float64) for k, v in prm.items()}
+    slot = np.arange(rows, dtype=np.int32)
+    threads = oracle.default_threads()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(ssm, slot, xbc, dt, o["A"], conv_pool=conv, conv_w=o["conv_w"], D=o["D"],
+                      dt_bias=o["dt_bias"], z=z, n_groups=G, nthreads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = n * rows * DECODE_BYTES_PER_TOKEN_LAYER / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} x {rows} rows of one Nemotron-H-8B decode layer (fp64 C oracle, {el:.1f} s)",
+            "token_layers_per_s": n * rows / el}
+
+
+def run_gpu(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from recurrent_state_update_gb300 import build as bld
+    bld.build()
+    hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
+
+    dec = DecodeWorkload(torch, rank, DECODE["layers"], DECODE["batch"], DECODE["pool"])
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        dec.step()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ms = _time(torch, dec.step, args.steps, 0, dist)
+    ck = clocks.stop()
+    ms = _max_over_ranks(torch, dist, ms)
+    total_bytes = dec.bytes_per_step() * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    token_layers = DECODE["layers"] * DECODE["batch"] * world / (ms * 1e-3)
+    launch_ms = ms / dec.launches_per_step
+    achieved = DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER / (launch_ms * 1e-3) / 1e9
+
+    # end to end: pinned host inputs in, every layer's y out, inside the timed region
+    ms_e2e = _max_over_ranks(torch, dist, _time(torch, dec.step_e2e, args.steps, 2, dist))
+    e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
+    del dec
+    torch.cuda.empty_cache()
+
+    pre = PrefillWorkload(torch, rank)
+    ms_pre = _max_over_ranks(torch, dist, _time(torch, pre.step, args.steps, max(args.warmup, 3), dist))
+    fl = prefill_flops(pre.lengths, PREFILL["chunk"])
+    by = prefill_bytes(pre.T, len(pre.lengths), pre.n_state_writes)
+    prefill = {
+        "tokens_per_s": pre.T * world / (ms_pre * 1e-3), "ms_per_layer": ms_pre,
+        "workload": PREFILL["name"], "lengths": [int(v) for v in pre.lengths],
+        "hbm_frac": by / (ms_pre * 1e-3) / 1e9 / hbm_peak,
+        "tensor_frac": fl / (ms_pre * 1e-3) / 1e12 / bf16_peak,
+        "algorithmic_bytes": by, "algorithmic_flops": fl,
+        "launches_per_layer": 6,
+    }
+    del pre
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode()
+
+    if rank == 0:
+        line = {
+            "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
+            "config": {"workload": DECODE["name"], "layers": DECODE["layers"], "global_batch": DECODE["batch"] * world,
+                       "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
+                       "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
+                       "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"},
+            "token_layers_per_s": token_layers,
+            "roofline": {"bound": "hbm", "kernel": "k_decode", "achieved": achieved, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_src,
+                         "traffic": _profile_traffic("decode_nemotron_b256"),
+                         "algorithmic_bytes_per_launch": DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER,
+                         "avg_launch_ms": launch_ms},
+            "e2e": e2e,
+            "gpu_launches": args.steps * DECODE["layers"],
+            "clocks": ck,
+            "prefill": prefill,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows = 8
+    # one step = the oracle on `rows` rows of one decode layer
+    import oracle
+    seed = DECODE["seed"] * 1000
+    g = wl.rng(seed, 0)
+    prm = wl.layer_params(g, SHAPE)
+    inp = wl.decode_inputs(g, SHAPE, prm, rows, 1, wl.BF16)
+    st = wl.initial_states(wl.rng(seed, 99), SHAPE, rows, wl.BF16, wl.BF16)
+    ssm, conv = wl.upcast(st["ssm"], wl.BF16), wl.upcast(st["conv"], wl.BF16)
+    xbc, z = wl.upcast(inp["xbc"], wl.BF16), wl.upcast(inp["z"], wl.BF16).reshape(rows, 1, H, P)
+    dt = inp["dt"].astype(np.float64)
+    o = {k: v.astype(np.float64) for k, v in prm.items()}
+    slot = np.arange(rows, dtype=np.int32)
+    threads = oracle.default_threads()
+
+    def step():
+        oracle.decode(ssm, slot, xbc, dt, o["A"], conv_pool=conv, conv_w=o["conv_w"], D=o["D"],
+                      dt_bias=o["dt_bias"], z=z, n_groups=G, nthreads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    value = rows * DECODE_BYTES_PER_TOKEN_LAYER / (el / args.steps) / 1e9
+    sample = f"{rows} rows of one Nemotron-H-8B decode layer per step (fp64 C oracle)"
+    line = {
+        "impl": "reference",
+        "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
+        "value": value, "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": DECODE["name"], "sample_rows_per_step": rows},
+        "token_layers_per_s": rows / (el / args.steps),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * mamba_state.h -- C ABI of libmamba_state.so: the Mamba2 recurrent-state update over a
+ * slot-indexed state pool, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (page title, section / equation):
+ *  [P1] "Hybrid SSM / Mamba models and non-KV state" (mlinterviewnotes.com):
+ *       - the Mamba2 state shapes: conv state (d_conv, W-1+num_spec) with
+ *         d_conv = d_inner + 2*n_groups*d_state, temporal state (nheads, head_dim, d_state);
+ *       - the slot pool: one dense tensor per state object indexed [layer, slot, ...], plus a
+ *         padding slot, requests holding an integer slot id;
+ *       - the decode call selective_state_update(ssm_state, x, dt, A, B, C, D, z, dt_bias,
+ *         dt_softplus, state_batch_indices, out);
+ *       - the prefill call mamba_chunk_scan_combined(x viewed (1, T, H, P), dt, A, ...) and the
+ *         chunked-prefill state hand-off (has_initial_states);
+ *       - align-mode checkpoints "at position i * block_size";
+ *       - the block-table "none"/"align" columns 1 + num_speculative_blocks (speculative
+ *         decode keeps 1 + num_spec state pages per request).
+ *  [P4] echobase "Mamba" notes, the Mamba block equations:
+ *         x = SiLU(Conv1d(x')),  Delta_t = Softplus(.),
+ *         h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,  y_t = C_t h_t,  y_hat = y (.) SiLU(z),
+ *       the classic output y_t = C h_t + D x_t, and the SSD form Y = (M (.) L) X with
+ *         M_ij = C_i (prod_{k=j+1..i} Abar_k) Bbar_j,  L the causal mask.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no
+ *    memory.  Every tensor is dense row-major in the layout given beside it.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and never synchronise the host.
+ *  - Errors the host can see (null required pointer, unsupported shape or dtype, a pointer
+ *    not 16-byte aligned, a launch failure) return a negative mamba_status and launch
+ *    nothing.  Errors that depend on device data (a slot id outside the pool, an accept
+ *    length out of range, bad cu_seqlens) are found in the kernel: the affected unit is
+ *    left untouched and a MAMBA_ERR_* bit is OR-ed into *err_word (a device int32 the
+ *    caller zeroes and reads; it may be NULL to ignore such errors).
+ *  - Slot ids within one call must be distinct (also across slot_ids and scratch_slots);
+ *    the result is undefined otherwise.  Slot id -1 marks a padding row: its state and its
+ *    output rows are not touched.
+ *  - Head h uses group g(h) = h / (nheads / n_groups).  xBC channels are ordered
+ *    [x (nheads*head_dim) | B (n_groups*d_state) | C (n_groups*d_state)].
+ */
+#ifndef MAMBA_STATE_H
+#define MAMBA_STATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_EINVAL = -1,       /* bad argument: null pointer, negative size, inconsistent shape */
+    MAMBA_EUNSUPPORTED = -2, /* valid but not compiled: head_dim/d_state/dtype combination */
+    MAMBA_ECUDA = -3,        /* a CUDA runtime call or kernel launch failed */
+    MAMBA_EALIGN = -4,       /* a pointer or stride breaks the 16-byte alignment rule */
+    MAMBA_ENOSPACE = -5      /* a caller-provided buffer is too small */
+} mamba_status;
+
+typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
+
+/* Data-dependent error bits OR-ed into *err_word. */
+#define MAMBA_ERR_SLOT_RANGE 0x1   /* a slot / scratch / checkpoint slot id outside [0, num_slots) */
+#define MAMBA_ERR_ACCEPT_RANGE 0x2 /* an accept length outside [0, ntok] */
+#define MAMBA_ERR_SEQLENS 0x4      /* cu_seqlens not non-decreasing from 0 to total_tokens */
+
+/* One Mamba2 layer [P1 state shapes, P4 block equations]. */
+typedef struct mamba_layer_desc {
+    int32_t nheads;      /* H */
+    int32_t head_dim;    /* P */
+    int32_t d_state;     /* N */
+    int32_t n_groups;    /* G; nheads % n_groups == 0 */
+    int32_t conv_kernel; /* W, 2..8 */
+    int32_t num_spec;    /* extra conv-state columns for speculative tokens, >= 0 */
+    int32_t state_dtype; /* mamba_dtype of the SSM (temporal) state pool */
+    int32_t conv_dtype;  /* mamba_dtype of the conv state pool; must equal act_dtype */
+    int32_t act_dtype;   /* mamba_dtype of xBC, x, B, C, z and y */
+    int32_t dt_dtype;    /* mamba_dtype of dt */
+} mamba_layer_desc;
+
+/* ---------------------------------------------------------------------------------------- */
+/* sizes and status                                                                         */
+/* ---------------------------------------------------------------------------------------- */
+
+/* conv_dim = nheads*head_dim + 2*n_groups*d_state [P1 state shapes]; -1 on a bad desc. */
+int32_t mamba_conv_dim(const mamba_layer_desc *desc);
+
+/* Bytes of one slot of the SSM state, nheads*head_dim*d_state*sizeof(state_dtype)
+ * [P1 temporal state]; -1 on a bad desc. */
+int64_t mamba_ssm_state_bytes(const mamba_layer_desc *desc);
+
+/* Bytes of one slot of the conv state, conv_dim*(conv_kernel-1+num_spec)*sizeof(conv_dtype)
+ * [P1 conv state]; -1 on a bad desc. */
+int64_t mamba_conv_state_bytes(const mamba_layer_desc *desc);
+
+/* MAMBA_OK when the decode kernels are compiled for this desc, else MAMBA_EUNSUPPORTED or
+ * MAMBA_EINVAL.  Compiled: (head_dim, d_state) in {(16,16), (32,64), (64,64), (64,128),
+ * (128,128)}, state f32 or bf16, act bf16 or f32, dt f32 or bf16. */
+int mamba_decode_supported(const mamba_layer_desc *desc);
+
+/* Human-readable name of a mamba_status. */
+const char *mamba_status_string(int status);
+
+/* ---------------------------------------------------------------------------------------- */
+/* decode                                                                                   */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * mamba_conv_update -- causal depthwise conv1d + SiLU over ntok new tokens per request,
+ * updating the conv state in place [P1 "a rolling window of the last W-1 token activations";
+ * P4 x = SiLU(Conv1d(x'))].
+ *
+ *   conv_pool        (num_slots, ...) with slot s at conv_pool + s*conv_slot_stride elements;
+ *                    a slot holds (conv_dim, Wc) with Wc = conv_kernel-1+num_spec, each
+ *                    channel's Wc columns contiguous, oldest first.
+ *   slot_ids         (batch) int32, -1 = padding (row skipped, xbc_out row not written).
+ *   xbc_in           (batch, ntok, conv_dim) act_dtype, raw inputs.
+ *   conv_w           (conv_dim, conv_kernel) fp32; the newest input meets conv_w[c, W-1].
+ *   conv_b           (conv_dim) fp32 or NULL.
+ *   xbc_out          (batch, ntok, conv_dim) act_dtype: SiLU(conv + bias).  May not alias xbc_in.
+ * Token j's window is the last W-1 inputs before it followed by itself.  After the call the
+ * slot holds the last Wc inputs (shifted left by ntok, new inputs appended).
+ * Limits: 1 <= ntok <= 64, batch <= 65535.
+ */
+int mamba_conv_update(const mamba_layer_desc *desc, void *conv_pool, int64_t conv_slot_stride,
+                      int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
+                      const void *xbc_in, const float *conv_w, const float *conv_b, void *xbc_out,
+                      int32_t *err_word, void *stream);
+
+/*
+ * mamba_state_update -- the batched decode step [P1 selective_state_update call; P4 block
+ * equations]: for each row i with s = slot_ids[i] != -1, for tokens j = 0..ntok-1 in order,
+ * for each head h (group g):
+ *     Delta = softplus(dt[i,j,h] + dt_bias[h])   (dt + dt_bias when dt_softplus == 0)
+ *     hst[p,n] <- exp(Delta*A[h]) * hst[p,n] + Delta * B[g,n] * x[h,p]
+ *     y[i,j,h,p] = sum_n C[g,n] * hst[p,n] + D[h]*x[h,p];   y *= SiLU(z[i,j,h,p]) if z
+ * where x | B | C are the xBC channels after the conv (when conv_pool != NULL the conv of
+ * mamba_conv_update is fused in and the conv state is updated in place; when NULL, xbc is
+ * taken as already convolved).
+ *
+ *   ssm_pool         slot s at ssm_pool + s*ssm_slot_stride elements: (nheads, head_dim,
+ *                    d_state) state_dtype, d_state contiguous.  Read, updated in fp32, and
+ *                    written back (bf16: round to nearest even).
+ *   conv_pool        as in mamba_conv_update, or NULL.
+ *   conv_w, conv_b   as in mamba_conv_update (conv_w required when conv_pool != NULL).
+ *   slot_ids         (batch) int32, -1 = padding.
+ *   scratch_slots    (batch, ntok) int32 or NULL.  When given (speculative decode), the state
+ *                    after token j is written to slot scratch_slots[i, j] and slot_ids[i] is
+ *                    NOT written; when NULL the state after the last token is written back to
+ *                    slot_ids[i].
+ *   xbc              (batch, ntok, conv_dim) act_dtype.
+ *   dt               (batch, ntok, nheads) dt_dtype.
+ *   A                (nheads) fp32, required.   D, dt_bias: (nheads) fp32 or NULL.
+ *   z                (batch, ntok, nheads*head_dim) act_dtype or NULL (no gate).
+ *   y                (batch, ntok, nheads*head_dim) act_dtype.
+ * Limits: 1 <= ntok <= 8, batch <= 65535.
+ * Alignment: ssm_pool and the SSM slot stride in bytes must be multiples of 16; the other
+ * tensors must be aligned to their element size (MAMBA_EALIGN otherwise).
+ */
+int mamba_state_update(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                       int64_t num_slots, void *conv_pool, int64_t conv_slot_stride,
+                       const float *conv_w, const float *conv_b, const int32_t *slot_ids,
+                       const int32_t *scratch_slots, int32_t batch, int32_t ntok, const void *xbc,
+                       const void *dt, const float *A, const float *D, const float *dt_bias,
+                       int32_t dt_softplus, const void *z, void *y, int32_t *err_word, void *stream);
+
+/*
+ * mamba_spec_commit -- after a speculative mamba_state_update of ntok draft tokens with
+ * scratch slots, keep the first accept_len[i] tokens of row i [P1: 1 + num_speculative_blocks
+ * state pages per request so a rejected suffix rolls back]:
+ *   - accept a >= 1: the state in scratch_slots[i, a-1] is copied into slot_ids[i];
+ *     a == 0 leaves slot_ids[i] unchanged;
+ *   - conv_pool (may be NULL): the slot's conv state, which the speculative step left holding
+ *     the last Wc inputs up to draft token ntok, is moved right by ntok - a columns so its
+ *     last W-1 columns end at accepted token a; the ntok - a freed columns are zeroed.
+ *     Requires ntok <= num_spec.
+ * accept_len: (batch) int32 in [0, ntok]; out of range -> MAMBA_ERR_ACCEPT_RANGE, row skipped.
+ */
+int mamba_spec_commit(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                      int64_t num_slots, void *conv_pool, int64_t conv_slot_stride,
+                      const int32_t *slot_ids, const int32_t *scratch_slots,
+                      const int32_t *accept_len, int32_t batch, int32_t ntok, int32_t *err_word,
+                      void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* chunked prefill                                                                          */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * Bytes of device workspace mamba_chunk_scan needs for these sizes (0 on a bad argument).
+ */
+size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *desc, int32_t total_tokens,
+                                        int32_t nseq, int32_t chunk);
+
+/*
+ * mamba_chunk_scan -- varlen chunked prefill in the SSD form [P1 mamba_chunk_scan_combined,
+ * "masked matmul on tensor cores ... stitched with a small inter-chunk scan"; P4 Y = (M (.) L) X].
+ * Sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]) of x; its tokens are split into
+ * chunks of `chunk` tokens from its first token (the last chunk may be partial).  Per head:
+ *     y_t = C_t . h_t + D*x_t  (then * SiLU(z_t) if z),  h_t = exp(Delta_t A) h_{t-1} + Delta_t x_t B_t^T
+ * with h_{-1} = the state in slot_ids[s] when has_initial_state[s] != 0, else 0
+ * [P1 chunked prefill is a state hand-off].  After the call slot_ids[s] holds the state after
+ * the sequence's last token; when ckpt_slots is given, ckpt_slots[s, k-1] (k >= 1, -1 = skip)
+ * receives the state after the first k*ckpt_interval tokens of the sequence [P1 align mode:
+ * states cached at positions i * block_size].
+ *
+ *   ssm_pool, ssm_slot_stride, num_slots   as in mamba_state_update.
+ *   cu_seqlens       (nseq + 1) int32, non-decreasing, cu_seqlens[0] = 0,
+ *                    cu_seqlens[nseq] = total_tokens.
+ *   slot_ids         (nseq) int32 (-1: the sequence's outputs are computed, no state written).
+ *   has_initial_state (nseq) uint8 or NULL (all zero).
+ *   ckpt_slots       (nseq, max_ckpt) int32 or NULL;  ckpt_interval must be a positive
+ *                    multiple of chunk when given.
+ *   chunk            tokens per chunk; 256 is compiled.
+ *   x                (total_tokens, nheads, head_dim) act_dtype (bf16 only).
+ *   dt               (total_tokens, nheads) dt_dtype.
+ *   A (nheads) fp32;  D, dt_bias (nheads) fp32 or NULL.
+ *   B, C             (total_tokens, n_groups, d_state) act_dtype.
+ *   z                (total_tokens, nheads, head_dim) act_dtype or NULL.
+ *   y                (total_tokens, nheads, head_dim) act_dtype.
+ *   workspace        device buffer of at least mamba_chunk_scan_workspace_bytes(...) bytes,
+ *                    16-byte aligned (MAMBA_ENOSPACE when workspace_bytes is smaller).
+ */
+int mamba_chunk_scan(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                     int64_t num_slots, const int32_t *cu_seqlens, int32_t nseq,
+                     int32_t total_tokens, const int32_t *slot_ids,
+                     const uint8_t *has_initial_state, const int32_t *ckpt_slots,
+                     int32_t max_ckpt, int32_t ckpt_interval, int32_t chunk, const void *x,
+                     const void *dt, const float *A, const void *B, const void *C, const float *D,
+                     const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
+                     void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_STATE_H */

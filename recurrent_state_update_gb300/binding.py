@@ -1,0 +1,197 @@
+"""Thin ctypes binding of libmamba_state.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch CUDA tensors (or
+None for nullable arguments), passes their device pointers and sizes, and raises
+:class:`MambaError` on a non-zero status.  All arithmetic happens in the CUDA kernels; there is
+no CPU path.  Loading fails loudly when the library has not been built.
+
+Layouts are the ones the C header documents (include/mamba_state.h); tensors must be
+contiguous except the pools, whose slot stride is taken from ``stride(0)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import workloads as wl
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmamba_state.so")
+
+MAMBA_OK, MAMBA_EINVAL, MAMBA_EUNSUPPORTED, MAMBA_ECUDA, MAMBA_EALIGN, MAMBA_ENOSPACE = 0, -1, -2, -3, -4, -5
+MAMBA_F32, MAMBA_BF16 = 0, 1
+MAMBA_ERR_SLOT_RANGE, MAMBA_ERR_ACCEPT_RANGE, MAMBA_ERR_SEQLENS = 0x1, 0x2, 0x4
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class LayerDesc(ctypes.Structure):
+    """Mirror of ``mamba_layer_desc``."""
+
+    _fields_ = [(n, ctypes.c_int32) for n in ("nheads", "head_dim", "d_state", "n_groups", "conv_kernel",
+                                              "num_spec", "state_dtype", "conv_dtype", "act_dtype",
+                                              "dt_dtype")]
+
+
+def layer_desc(shape: "wl.LayerShape", state: str = wl.BF16, act: str = wl.BF16, dt: str = wl.F32,
+               conv: str | None = None) -> LayerDesc:
+    code = wl.DTYPE_CODE
+    return LayerDesc(shape.nheads, shape.head_dim, shape.d_state, shape.n_groups, shape.conv_kernel,
+                     shape.num_spec, code[state], code[conv or act], code[act], code[dt])
+
+
+_lock = threading.Lock()
+_lib = None
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_dp = ctypes.POINTER(LayerDesc)
+
+# (name, restype, argtypes) of every exported entry point
+SIGNATURES = {
+    "mamba_conv_dim": (_i32, [_dp]),
+    "mamba_ssm_state_bytes": (_i64, [_dp]),
+    "mamba_conv_state_bytes": (_i64, [_dp]),
+    "mamba_decode_supported": (ctypes.c_int, [_dp]),
+    "mamba_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mamba_conv_update": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mamba_state_update": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
+                                          _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "mamba_spec_commit": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
+    "mamba_chunk_scan_workspace_bytes": (_sz, [_dp, _i32, _i32, _i32]),
+    "mamba_chunk_scan": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
+}
+
+
+def lib():
+    """The loaded library; raises if it was not built (there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with recurrent_state_update_gb300.build.build()")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mamba_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != MAMBA_OK:
+        raise MambaError(rc, what)
+
+
+def _ptr(t):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _cptr(t):
+    if t is not None and not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return _ptr(t)
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------------------------------
+# sizes
+# ------------------------------------------------------------------------------------------
+
+def mamba_conv_dim(desc: LayerDesc) -> int:
+    return lib().mamba_conv_dim(ctypes.byref(desc))
+
+
+def mamba_ssm_state_bytes(desc: LayerDesc) -> int:
+    return lib().mamba_ssm_state_bytes(ctypes.byref(desc))
+
+
+def mamba_conv_state_bytes(desc: LayerDesc) -> int:
+    return lib().mamba_conv_state_bytes(ctypes.byref(desc))
+
+
+def mamba_decode_supported(desc: LayerDesc) -> int:
+    return lib().mamba_decode_supported(ctypes.byref(desc))
+
+
+def mamba_chunk_scan_workspace_bytes(desc: LayerDesc, total_tokens: int, nseq: int, chunk: int) -> int:
+    return lib().mamba_chunk_scan_workspace_bytes(ctypes.byref(desc), total_tokens, nseq, chunk)
+
+
+# ------------------------------------------------------------------------------------------
+# decode
+# ------------------------------------------------------------------------------------------
+
+def mamba_conv_update(desc: LayerDesc, conv_pool, slot_ids, xbc_in, conv_w, xbc_out, *, conv_b=None,
+                      err_word=None, stream=None):
+    """Causal conv1d + SiLU over (batch, ntok, conv_dim) inputs, conv state updated in place."""
+    batch, ntok = int(slot_ids.shape[0]), int(xbc_in.shape[1])
+    rc = lib().mamba_conv_update(ctypes.byref(desc), _ptr(conv_pool), conv_pool.stride(0), conv_pool.shape[0],
+                                 _cptr(slot_ids), batch, ntok, _cptr(xbc_in), _cptr(conv_w), _cptr(conv_b),
+                                 _cptr(xbc_out), _ptr(err_word), _stream(stream))
+    _check(rc, "mamba_conv_update")
+
+
+def mamba_state_update(desc: LayerDesc, ssm_pool, slot_ids, xbc, dt, A, y, *, conv_pool=None, conv_w=None,
+                       conv_b=None, scratch_slots=None, D=None, dt_bias=None, dt_softplus=True, z=None,
+                       err_word=None, stream=None):
+    """The batched decode step (conv fused when ``conv_pool`` is given), in place on the pools."""
+    batch, ntok = int(slot_ids.shape[0]), int(xbc.shape[1])
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    rc = lib().mamba_state_update(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                                  _ptr(conv_pool), conv_stride, _cptr(conv_w), _cptr(conv_b), _cptr(slot_ids),
+                                  _cptr(scratch_slots), batch, ntok, _cptr(xbc), _cptr(dt), _cptr(A), _cptr(D),
+                                  _cptr(dt_bias), int(bool(dt_softplus)), _cptr(z), _cptr(y), _ptr(err_word),
+                                  _stream(stream))
+    _check(rc, "mamba_state_update")
+
+
+def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept_len, *, conv_pool=None,
+                      err_word=None, stream=None):
+    """Keep accept_len[i] of the speculative tokens: copy the scratch state, re-seat the conv window."""
+    batch, ntok = int(scratch_slots.shape[0]), int(scratch_slots.shape[1])
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    rc = lib().mamba_spec_commit(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                                 _ptr(conv_pool), conv_stride, _cptr(slot_ids), _cptr(scratch_slots),
+                                 _cptr(accept_len), batch, ntok, _ptr(err_word), _stream(stream))
+    _check(rc, "mamba_spec_commit")
+
+
+# ------------------------------------------------------------------------------------------
+# prefill
+# ------------------------------------------------------------------------------------------
+
+def mamba_chunk_scan(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x, dt, A, B, C, y, workspace, *,
+                     has_initial_state=None, ckpt_slots=None, ckpt_interval=0, chunk=256, D=None, dt_bias=None,
+                     dt_softplus=True, z=None, err_word=None, stream=None):
+    """Varlen chunked prefill (SSD form); final states and checkpoints written into the pool."""
+    nseq = int(cu_seqlens.shape[0]) - 1
+    total = int(x.shape[0])
+    max_ckpt = int(ckpt_slots.shape[1]) if ckpt_slots is not None else 0
+    rc = lib().mamba_chunk_scan(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                                _cptr(cu_seqlens), nseq, total, _cptr(slot_ids), _cptr(has_initial_state),
+                                _cptr(ckpt_slots), max_ckpt, int(ckpt_interval), int(chunk), _cptr(x), _cptr(dt),
+                                _cptr(A), _cptr(B), _cptr(C), _cptr(D), _cptr(dt_bias), int(bool(dt_softplus)),
+                                _cptr(z), _cptr(y), _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _ptr(err_word), _stream(stream))
+    _check(rc, "mamba_chunk_scan")

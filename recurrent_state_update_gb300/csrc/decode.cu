@@ -1,0 +1,567 @@
+// decode.cu -- the batched decode step of the Mamba2 state update over a slot pool.
+//
+// Operations ("Hybrid SSM / Mamba models and non-KV state", state shapes and the decode call
+// selective_state_update; echobase "Mamba" notes, block equations):
+//   conv:   x|B|C = SiLU(causal depthwise conv1d over [conv state | new token])
+//   step:   Delta = softplus(dt + dt_bias),  h <- exp(Delta*A) h + Delta * x B^T
+//   out:    y = C.h + D*x,  y *= SiLU(z)
+//
+// Design (GB300): the state update is a pure HBM stream (about 1.25 flop per byte at bf16),
+// so the kernel is built around moving each (slot, head) state tile of head_dim x d_state once
+// in and once out with 16-byte coalesced accesses and evict-first cache hints, while the
+// small per-group work (conv of x|B|C, Delta, exp) runs out of shared memory.
+//
+//  - One CTA per (row, group): the group's heads share one B and C, so the conv of the group's
+//    B and C channels is done once and the CTA owns every conv-state column it writes (no two
+//    CTAs touch one slot's conv channels).
+//  - Within the CTA a head tile is split over TH threads: a row of d_state elements is VR
+//    consecutive lanes, each holding one 16-byte vector per pass; each thread keeps its part
+//    of the tile in fp32 registers across the (speculative) tokens.
+//  - C.h is a row sum over VR lanes: a reduce-scatter of the per-pass partials (halving the
+//    values exchanged at each shuffle step) leaves one row total per lane pair.
+//  - The first head's state loads are issued before the conv phase so they are in flight
+//    while the CTA convolves.
+#include "common.cuh"
+
+namespace ms {
+
+// ---------------------------------------------------------------------------------------
+// tile geometry of one head's (head_dim x d_state) state
+// ---------------------------------------------------------------------------------------
+
+template <typename StateT, int P, int N>
+struct Tile {
+    static constexpr int VEC = Vec16<StateT>::n;  // elements per 16-byte vector
+    static constexpr int VR = N / VEC;            // vectors (= lanes) per state row
+    static constexpr int TV = P * N / VEC;        // vectors per head tile
+    static constexpr int PR = TV / 128;
+    static constexpr int PASSES = PR < 1 ? 1 : (PR > 8 ? 8 : PR);  // vectors per thread
+    static constexpr int TH = TV / PASSES;        // threads per head tile
+    static constexpr int RP = TH / VR;            // rows covered per pass
+    static_assert(N % VEC == 0, "d_state must fill whole 16-byte vectors");
+    static_assert(TV % PASSES == 0 && TH % 32 == 0 && TH <= 512, "tile must split into warps");
+    static_assert(VR <= 32 && (VR & (VR - 1)) == 0, "a state row must sit inside one warp");
+    static_assert(PASSES <= VR, "reduce-scatter needs at least as many lanes as partials");
+};
+
+// Reduce-scatter of CNT partials over the lanes that differ in bits OFF, OFF/2, ..., 1.
+// Halving steps exchange half the values; once one value is left the rest are butterflies.
+// On return v[0] is the full sum for partial index `idx`.
+template <int CNT, int OFF>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int lane, int &idx) {
+        if constexpr (OFF == 0) {
+            return;
+        } else if constexpr (CNT > 1) {
+            constexpr int HALF = CNT / 2;
+            const bool upper = (lane & OFF) != 0;
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                const float send = upper ? v[k] : v[k + HALF];
+                const float keep = upper ? v[k + HALF] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+            }
+            if (upper) idx += HALF;
+            ReduceScatter<HALF, OFF / 2>::run(v, lane, idx);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
+            ReduceScatter<1, OFF / 2>::run(v, lane, idx);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// conv phase: block-cooperative conv1d + SiLU over a set of channel ranges
+// ---------------------------------------------------------------------------------------
+
+// Up to three contiguous global-channel ranges, numbered back to back as local channels.
+struct ChanRanges {
+    int lo[3];
+    int len[3];
+    int total;
+};
+
+__device__ __forceinline__ int local_to_global(const ChanRanges &r, int lc) {
+    if (lc < r.len[0]) return r.lo[0] + lc;
+    lc -= r.len[0];
+    if (lc < r.len[1]) return r.lo[1] + lc;
+    return r.lo[2] + (lc - r.len[1]);
+}
+
+// Stages the old conv state and the raw inputs in shared memory, writes SiLU(conv) of every
+// (token, local channel) to xs[ntok][LC], and writes the shifted conv state back.
+//   cstate: the slot's conv state (conv_dim x Wc, oldest column first), global memory.
+//   u_row:  this row's raw inputs, (ntok x Cd).
+template <typename ActT>
+__device__ __forceinline__ void conv_phase(const ChanRanges &cr, ActT *cstate, int Wc, int W, int ntok,
+                                           const ActT *u_row, int Cd, const float *__restrict__ w,
+                                           const float *__restrict__ b, ActT *cs, float *uraw,
+                                           float *xs) {
+    const int tid = threadIdx.x, nthr = blockDim.x, LC = cr.total;
+    int base = 0;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        const ActT *src = cstate + (int64_t)cr.lo[r] * Wc;
+        for (int e = tid; e < cr.len[r] * Wc; e += nthr) cs[base * Wc + e] = src[e];
+        base += cr.len[r];
+    }
+    for (int idx = tid; idx < ntok * LC; idx += nthr) {
+        const int j = idx / LC, lc = idx - j * LC;
+        uraw[idx] = to_f32(u_row[(int64_t)j * Cd + local_to_global(cr, lc)]);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < ntok * LC; idx += nthr) {
+        const int j = idx / LC, lc = idx - j * LC;
+        const int c = local_to_global(cr, lc);
+        float v = b ? b[c] : 0.0f;
+        for (int k = 0; k < W; ++k) {
+            const int m = Wc + j - (W - 1) + k;  // index into [old state (Wc) | new tokens]
+            const float val = m < Wc ? to_f32(cs[lc * Wc + m]) : uraw[(m - Wc) * LC + lc];
+            v = fmaf(w[(int64_t)c * W + k], val, v);
+        }
+        xs[idx] = silu_f(v);
+    }
+    // new column k is input ntok + k of [old state | new tokens]
+    base = 0;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        ActT *dst = cstate + (int64_t)cr.lo[r] * Wc;
+        for (int e = tid; e < cr.len[r] * Wc; e += nthr) {
+            const int lcl = e / Wc, k = e - lcl * Wc, m = ntok + k;
+            dst[e] = m < Wc ? cs[(base + lcl) * Wc + m]
+                            : from_f32<ActT>(uraw[(m - Wc) * LC + base + lcl]);
+        }
+        base += cr.len[r];
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// fused decode kernel
+// ---------------------------------------------------------------------------------------
+
+struct DecodeArgs {
+    void *ssm_pool;
+    int64_t ssm_stride;
+    int64_t num_slots;
+    void *conv_pool;
+    int64_t conv_stride;
+    const float *conv_w, *conv_b;
+    const int32_t *slot, *scratch;
+    int32_t batch, ntok;
+    const void *xbc, *dt;
+    int dt_bf16;
+    const float *A, *D, *dt_bias;
+    int dt_softplus;
+    const void *z;
+    void *y;
+    int32_t *err;
+    int H, G, HG, W, Wc, Cd;
+};
+
+// Shared-memory floats the decode kernel needs (the conv staging area follows, in ActT).
+__host__ __device__ inline int decode_smem_floats(int ntok, int LC, int HG, int P, bool conv) {
+    return ntok * LC + (conv ? ntok * LC : 0) + 2 * ntok * HG + ntok * HG * P;
+}
+
+template <typename StateT, int P, int N>
+__device__ __forceinline__ void load_tile(uint4 (&raw)[Tile<StateT, P, N>::PASSES], const StateT *base,
+                                          int th) {
+    using TL = Tile<StateT, P, N>;
+#pragma unroll
+    for (int pass = 0; pass < TL::PASSES; ++pass)
+        raw[pass] = __ldcs(reinterpret_cast<const uint4 *>(base) + pass * TL::TH + th);
+}
+
+template <typename StateT, int P, int N>
+__device__ __forceinline__ void store_tile(const float (&st)[Tile<StateT, P, N>::PASSES][Tile<StateT, P, N>::VEC],
+                                           StateT *base, int th) {
+    using TL = Tile<StateT, P, N>;
+#pragma unroll
+    for (int pass = 0; pass < TL::PASSES; ++pass)
+        __stcs(reinterpret_cast<uint4 *>(base) + pass * TL::TH + th, pack16(st[pass]));
+}
+
+template <typename StateT, typename ActT, int P, int N, int NT>
+__global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
+    using TL = Tile<StateT, P, N>;
+    constexpr int VEC = TL::VEC, VR = TL::VR, TH = TL::TH, RP = TL::RP, PASSES = TL::PASSES;
+    const int g = blockIdx.x, i = blockIdx.y;
+    const int ntok = NT > 0 ? NT : a.ntok;
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+
+    const int32_t s = a.slot[i];
+    if (s < 0) return;  // padding row
+    bool bad = s >= a.num_slots;
+    if (a.scratch)
+        for (int j = 0; j < ntok; ++j) {
+            const int32_t d = a.scratch[(int64_t)i * ntok + j];
+            bad |= d < -1 || d >= a.num_slots;
+        }
+    if (bad) {
+        if (tid == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+        return;
+    }
+
+    const int HG = a.HG, LC = HG * P + 2 * N;
+    const bool conv = a.conv_pool != nullptr;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float *xs = reinterpret_cast<float *>(smem_raw);  // [ntok][LC] x | B | C after the conv
+    float *uraw = xs + ntok * LC;                      // [ntok][LC] raw inputs (conv only)
+    float *dl = uraw + (conv ? ntok * LC : 0);         // [ntok][HG] Delta
+    float *da = dl + ntok * HG;                        // [ntok][HG] exp(Delta*A)
+    float *ys = da + ntok * HG;                        // [ntok][HG*P] C.h
+    ActT *cs = reinterpret_cast<ActT *>(ys + ntok * HG * P);  // [LC][Wc] old conv state
+
+    // first head tile's loads go out before the conv phase
+    const int hs = tid / TH, th = tid - hs * TH, NHS = nthr / TH;
+    StateT *grp = static_cast<StateT *>(a.ssm_pool) + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
+    uint4 raw[PASSES];
+    int hl = hs;
+    if (hl < HG) load_tile<StateT, P, N>(raw, grp + (int64_t)hl * P * N, th);
+
+    const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * ntok * a.Cd;
+    const int HP = a.H * P, GN = a.G * N;
+    ChanRanges cr;
+    cr.lo[0] = g * HG * P;    cr.len[0] = HG * P;
+    cr.lo[1] = HP + g * N;    cr.len[1] = N;
+    cr.lo[2] = HP + GN + g * N; cr.len[2] = N;
+    cr.total = LC;
+    if (conv) {
+        conv_phase<ActT>(cr, static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride, a.Wc, a.W,
+                         ntok, u_row, a.Cd, a.conv_w, a.conv_b, cs, uraw, xs);
+    } else {
+        for (int idx = tid; idx < ntok * LC; idx += nthr) {
+            const int j = idx / LC, lc = idx - j * LC;
+            xs[idx] = to_f32(u_row[(int64_t)j * a.Cd + local_to_global(cr, lc)]);
+        }
+    }
+    for (int idx = tid; idx < ntok * HG; idx += nthr) {
+        const int j = idx / HG, h = g * HG + (idx - j * HG);
+        const float sdt = load_scalar(a.dt, ((int64_t)i * ntok + j) * a.H + h, a.dt_bf16) +
+                          (a.dt_bias ? a.dt_bias[h] : 0.0f);
+        const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
+        dl[idx] = delta;
+        da[idx] = expf(delta * a.A[h]);
+    }
+    __syncthreads();
+
+    const int rsub = th / VR, n0 = (th - rsub * VR) * VEC;
+    for (; hl < HG; hl += NHS) {  // warp-uniform: TH is a multiple of 32
+        float st[PASSES][VEC];
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) unpack16(raw[pass], st[pass]);
+        for (int j = 0; j < ntok; ++j) {
+            const float dA = da[j * HG + hl], dlt = dl[j * HG + hl];
+            const float *xj = xs + j * LC;
+            float Bv[VEC], Cv[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(xj + HG * P + n0 + e);
+                const float4 c4 = *reinterpret_cast<const float4 *>(xj + HG * P + N + n0 + e);
+                Bv[e] = b4.x; Bv[e + 1] = b4.y; Bv[e + 2] = b4.z; Bv[e + 3] = b4.w;
+                Cv[e] = c4.x; Cv[e + 1] = c4.y; Cv[e + 2] = c4.z; Cv[e + 3] = c4.w;
+            }
+            float part[PASSES];
+#pragma unroll
+            for (int pass = 0; pass < PASSES; ++pass) {
+                const float dtx = dlt * xj[hl * P + pass * RP + rsub];
+                float acc = 0.0f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    st[pass][e] = fmaf(dA, st[pass][e], dtx * Bv[e]);
+                    acc = fmaf(Cv[e], st[pass][e], acc);
+                }
+                part[pass] = acc;
+            }
+            int idx = 0;
+            ReduceScatter<PASSES, VR / 2>::run(part, lane, idx);
+            if ((lane & (VR / PASSES - 1)) == 0) ys[j * HG * P + hl * P + idx * RP + rsub] = part[0];
+            if (a.scratch) {
+                const int32_t d = a.scratch[(int64_t)i * ntok + j];
+                if (d >= 0)
+                    store_tile<StateT, P, N>(st, static_cast<StateT *>(a.ssm_pool) + (int64_t)d * a.ssm_stride +
+                                                     (int64_t)(g * HG + hl) * P * N, th);
+            }
+        }
+        if (!a.scratch) store_tile<StateT, P, N>(st, grp + (int64_t)hl * P * N, th);
+        if (hl + NHS < HG) load_tile<StateT, P, N>(raw, grp + (int64_t)(hl + NHS) * P * N, th);
+    }
+    __syncthreads();
+
+    // y = C.h + D*x, gated by SiLU(z)
+    const ActT *zr = static_cast<const ActT *>(a.z);
+    ActT *yr = static_cast<ActT *>(a.y);
+    for (int idx = tid; idx < ntok * HG * P; idx += nthr) {
+        const int j = idx / (HG * P), lc = idx - j * HG * P;
+        const int h = g * HG + lc / P;
+        const float xv = xs[j * LC + lc];
+        float yv = ys[idx] + (a.D ? a.D[h] * xv : 0.0f);
+        const int64_t o = ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P + lc;
+        if (zr) yv *= silu_f(to_f32(zr[o]));
+        yr[o] = from_f32<ActT>(yv);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// standalone conv update
+// ---------------------------------------------------------------------------------------
+
+constexpr int CONV_CHANNELS = 256;
+
+struct ConvArgs {
+    void *conv_pool;
+    int64_t conv_stride, num_slots;
+    const int32_t *slot;
+    int32_t ntok;
+    const void *xbc_in;
+    const float *w, *b;
+    void *xbc_out;
+    int32_t *err;
+    int W, Wc, Cd;
+};
+
+template <typename ActT>
+__global__ void __launch_bounds__(256) k_conv_update(const ConvArgs a) {
+    const int cb = blockIdx.x, i = blockIdx.y, ntok = a.ntok;
+    const int32_t s = a.slot[i];
+    if (s < 0) return;
+    if (s >= a.num_slots) {
+        if (threadIdx.x == 0 && cb == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+        return;
+    }
+    ChanRanges cr;
+    cr.lo[0] = cb * CONV_CHANNELS;
+    cr.len[0] = min(CONV_CHANNELS, a.Cd - cr.lo[0]);
+    cr.lo[1] = cr.lo[2] = 0;
+    cr.len[1] = cr.len[2] = 0;
+    cr.total = cr.len[0];
+    const int LC = cr.total;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float *xs = reinterpret_cast<float *>(smem_raw);
+    float *uraw = xs + ntok * LC;
+    ActT *cs = reinterpret_cast<ActT *>(uraw + ntok * LC);
+    const ActT *u_row = static_cast<const ActT *>(a.xbc_in) + (int64_t)i * ntok * a.Cd;
+    conv_phase<ActT>(cr, static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride, a.Wc, a.W, ntok,
+                     u_row, a.Cd, a.w, a.b, cs, uraw, xs);
+    ActT *out = static_cast<ActT *>(a.xbc_out) + (int64_t)i * ntok * a.Cd;
+    for (int idx = threadIdx.x; idx < ntok * LC; idx += blockDim.x) {
+        const int j = idx / LC, lc = idx - j * LC;
+        out[(int64_t)j * a.Cd + cr.lo[0] + lc] = from_f32<ActT>(xs[idx]);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// speculative commit
+// ---------------------------------------------------------------------------------------
+
+struct CommitArgs {
+    void *ssm_pool;
+    int64_t ssm_stride, num_slots;
+    void *conv_pool;
+    int64_t conv_stride;
+    const int32_t *slot, *scratch, *accept;
+    int32_t ntok;
+    int32_t *err;
+    int H, tile_vecs, Cd, Wc;
+};
+
+// grid.x: H state-copy units (one head tile each) followed by conv units of CONV_CHANNELS
+// channels; grid.y: batch rows.  Every unit of a row applies the same validity checks so a bad
+// row is left entirely untouched.
+template <typename ActT>
+__global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
+    const int unit = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
+    const int32_t s = a.slot[i];
+    if (s < 0) return;
+    const int32_t acc = a.accept[i];
+    if (acc < 0 || acc > a.ntok) {
+        if (unit == 0 && tid == 0) flag_error(a.err, MAMBA_ERR_ACCEPT_RANGE);
+        return;
+    }
+    const int32_t src = acc >= 1 ? a.scratch[(int64_t)i * a.ntok + acc - 1] : 0;
+    if (s >= a.num_slots || src < 0 || src >= a.num_slots) {
+        if (unit == 0 && tid == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+        return;
+    }
+    if (unit < a.H) {
+        if (acc == 0) return;
+        const int64_t tile_bytes = (int64_t)a.tile_vecs * 16;
+        const uint4 *from = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.ssm_pool) +
+                                                            (int64_t)src * a.ssm_stride + unit * tile_bytes);
+        uint4 *to = reinterpret_cast<uint4 *>(static_cast<char *>(a.ssm_pool) + (int64_t)s * a.ssm_stride +
+                                              unit * tile_bytes);
+        for (int v = tid; v < a.tile_vecs; v += blockDim.x) __stcs(to + v, __ldcs(from + v));
+        return;
+    }
+    if (!a.conv_pool) return;
+    const int c0 = (unit - a.H) * CONV_CHANNELS;
+    const int nc = min(CONV_CHANNELS, a.Cd - c0), Wc = a.Wc, shift = a.ntok - acc;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ActT *cs = reinterpret_cast<ActT *>(smem_raw);
+    ActT *st = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride + (int64_t)c0 * Wc;
+    for (int e = tid; e < nc * Wc; e += blockDim.x) cs[e] = st[e];
+    __syncthreads();
+    for (int e = tid; e < nc * Wc; e += blockDim.x) {
+        const int c = e / Wc, k = e - c * Wc;
+        st[e] = k - shift >= 0 ? cs[c * Wc + k - shift] : from_f32<ActT>(0.0f);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+
+template <typename StateT, typename ActT, int P, int N>
+static int launch_decode_shape(const DecodeArgs &a, int ntok, int P_, int N_, cudaStream_t stream) {
+    using TL = Tile<StateT, P, N>;
+    const int LC = a.HG * P + 2 * N;
+    const bool conv = a.conv_pool != nullptr;
+    const size_t smem = sizeof(float) * (size_t)decode_smem_floats(ntok, LC, a.HG, P, conv) +
+                        (conv ? sizeof(ActT) * (size_t)LC * a.Wc : 0);
+    if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
+    int nhs = 256 / TL::TH;
+    if (nhs < 1) nhs = 1;
+    if (nhs > a.HG) nhs = a.HG;
+    const dim3 grid(a.G, a.batch), block(nhs * TL::TH);
+    auto kern = ntok == 1 ? k_decode<StateT, ActT, P, N, 1> : k_decode<StateT, ActT, P, N, 0>;
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return MAMBA_ECUDA;
+    }
+    kern<<<grid, block, smem, stream>>>(a);
+    return launch_status();
+}
+
+// The compiled (head_dim, d_state) tiles.
+#define MS_DECODE_SHAPES(X) X(16, 16) X(32, 64) X(64, 64) X(64, 128) X(128, 128)
+
+static bool decode_shape_compiled(int P, int N) {
+#define MS_SHAPE_CHECK(p, n) \
+    if (P == p && N == n) return true;
+    MS_DECODE_SHAPES(MS_SHAPE_CHECK)
+#undef MS_SHAPE_CHECK
+    return false;
+}
+
+template <typename StateT, typename ActT>
+static int dispatch_decode_shape(const DecodeArgs &a, int ntok, int P, int N, cudaStream_t stream) {
+#define MS_SHAPE_LAUNCH(p, n) \
+    if (P == p && N == n) return launch_decode_shape<StateT, ActT, p, n>(a, ntok, P, N, stream);
+    MS_DECODE_SHAPES(MS_SHAPE_LAUNCH)
+#undef MS_SHAPE_LAUNCH
+    return MAMBA_EUNSUPPORTED;
+}
+
+}  // namespace ms
+
+using namespace ms;
+
+extern "C" int mamba_decode_supported(const mamba_layer_desc *d) {
+    int rc = check_desc(d);
+    if (rc != MAMBA_OK) return rc;
+    if (!decode_shape_compiled(d->head_dim, d->d_state)) return MAMBA_EUNSUPPORTED;
+    if (d->conv_dtype != d->act_dtype) return MAMBA_EUNSUPPORTED;
+    return MAMBA_OK;
+}
+
+extern "C" int mamba_state_update(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride,
+                                  int64_t num_slots, void *conv_pool, int64_t conv_slot_stride,
+                                  const float *conv_w, const float *conv_b, const int32_t *slot_ids,
+                                  const int32_t *scratch_slots, int32_t batch, int32_t ntok,
+                                  const void *xbc, const void *dt, const float *A, const float *D,
+                                  const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
+                                  int32_t *err_word, void *stream) {
+    int rc = check_desc(d);
+    if (rc != MAMBA_OK) return rc;
+    if (batch < 0 || batch > 65535 || ntok < 1 || ntok > 8) return MAMBA_EINVAL;
+    if (batch == 0) return MAMBA_OK;
+    if (!ssm_pool || !slot_ids || !xbc || !dt || !A || !y) return MAMBA_EINVAL;
+    const int H = d->nheads, P = d->head_dim, N = d->d_state, G = d->n_groups;
+    const int Cd = mamba_conv_dim(d), Wc = d->conv_kernel - 1 + d->num_spec;
+    if (num_slots <= 0 || ssm_slot_stride < (int64_t)H * P * N) return MAMBA_EINVAL;
+    if (conv_pool && (!conv_w || conv_slot_stride < (int64_t)Cd * Wc)) return MAMBA_EINVAL;
+    if ((rc = mamba_decode_supported(d)) != MAMBA_OK) return rc;
+    const size_t sb = dtype_bytes(d->state_dtype);
+    if (!aligned16(ssm_pool) || ((size_t)ssm_slot_stride * sb) % 16 != 0) return MAMBA_EALIGN;
+    const size_t ab = dtype_bytes(d->act_dtype);
+    if (((uintptr_t)xbc | (uintptr_t)y | (uintptr_t)z | (uintptr_t)conv_pool) % ab != 0) return MAMBA_EALIGN;
+
+    DecodeArgs a;
+    a.ssm_pool = ssm_pool; a.ssm_stride = ssm_slot_stride; a.num_slots = num_slots;
+    a.conv_pool = conv_pool; a.conv_stride = conv_slot_stride; a.conv_w = conv_w; a.conv_b = conv_b;
+    a.slot = slot_ids; a.scratch = scratch_slots; a.batch = batch; a.ntok = ntok;
+    a.xbc = xbc; a.dt = dt; a.dt_bf16 = d->dt_dtype == MAMBA_BF16;
+    a.A = A; a.D = D; a.dt_bias = dt_bias; a.dt_softplus = dt_softplus != 0;
+    a.z = z; a.y = y; a.err = err_word;
+    a.H = H; a.G = G; a.HG = H / G; a.W = d->conv_kernel; a.Wc = Wc; a.Cd = Cd;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool sbf = d->state_dtype == MAMBA_BF16, abf = d->act_dtype == MAMBA_BF16;
+    if (sbf && abf) return dispatch_decode_shape<bf16, bf16>(a, ntok, P, N, st);
+    if (sbf && !abf) return dispatch_decode_shape<bf16, float>(a, ntok, P, N, st);
+    if (!sbf && abf) return dispatch_decode_shape<float, bf16>(a, ntok, P, N, st);
+    return dispatch_decode_shape<float, float>(a, ntok, P, N, st);
+}
+
+extern "C" int mamba_conv_update(const mamba_layer_desc *d, void *conv_pool, int64_t conv_slot_stride,
+                                 int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
+                                 const void *xbc_in, const float *conv_w, const float *conv_b, void *xbc_out,
+                                 int32_t *err_word, void *stream) {
+    int rc = check_desc(d);
+    if (rc != MAMBA_OK) return rc;
+    if (batch < 0 || batch > 65535 || ntok < 1 || ntok > 64) return MAMBA_EINVAL;
+    if (batch == 0) return MAMBA_OK;
+    if (!conv_pool || !slot_ids || !xbc_in || !conv_w || !xbc_out) return MAMBA_EINVAL;
+    if (d->conv_dtype != d->act_dtype) return MAMBA_EUNSUPPORTED;
+    const int Cd = mamba_conv_dim(d), Wc = d->conv_kernel - 1 + d->num_spec;
+    if (num_slots <= 0 || conv_slot_stride < (int64_t)Cd * Wc) return MAMBA_EINVAL;
+    const size_t ab = dtype_bytes(d->act_dtype);
+    if (((uintptr_t)conv_pool | (uintptr_t)xbc_in | (uintptr_t)xbc_out) % ab != 0) return MAMBA_EALIGN;
+    ConvArgs a;
+    a.conv_pool = conv_pool; a.conv_stride = conv_slot_stride; a.num_slots = num_slots;
+    a.slot = slot_ids; a.ntok = ntok; a.xbc_in = xbc_in; a.w = conv_w; a.b = conv_b;
+    a.xbc_out = xbc_out; a.err = err_word; a.W = d->conv_kernel; a.Wc = Wc; a.Cd = Cd;
+    const size_t smem = sizeof(float) * 2 * (size_t)ntok * CONV_CHANNELS + ab * (size_t)CONV_CHANNELS * Wc;
+    if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
+    const dim3 grid((Cd + CONV_CHANNELS - 1) / CONV_CHANNELS, batch), block(256);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto kern = d->act_dtype == MAMBA_BF16 ? k_conv_update<bf16> : k_conv_update<float>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MAMBA_ECUDA;
+    kern<<<grid, block, smem, st>>>(a);
+    return launch_status();
+}
+
+extern "C" int mamba_spec_commit(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride,
+                                 int64_t num_slots, void *conv_pool, int64_t conv_slot_stride,
+                                 const int32_t *slot_ids, const int32_t *scratch_slots,
+                                 const int32_t *accept_len, int32_t batch, int32_t ntok, int32_t *err_word,
+                                 void *stream) {
+    int rc = check_desc(d);
+    if (rc != MAMBA_OK) return rc;
+    if (batch < 0 || batch > 65535 || ntok < 1) return MAMBA_EINVAL;
+    if (batch == 0) return MAMBA_OK;
+    if (!ssm_pool || !slot_ids || !scratch_slots || !accept_len) return MAMBA_EINVAL;
+    const int H = d->nheads, P = d->head_dim, N = d->d_state;
+    const int Cd = mamba_conv_dim(d), Wc = d->conv_kernel - 1 + d->num_spec;
+    if (num_slots <= 0 || ssm_slot_stride < (int64_t)H * P * N) return MAMBA_EINVAL;
+    if (conv_pool && (conv_slot_stride < (int64_t)Cd * Wc || ntok > d->num_spec)) return MAMBA_EINVAL;
+    if (conv_pool && d->conv_dtype != d->act_dtype) return MAMBA_EUNSUPPORTED;
+    const size_t sb = dtype_bytes(d->state_dtype);
+    const int64_t tile_bytes = (int64_t)P * N * (int64_t)sb;
+    if (!aligned16(ssm_pool) || ((size_t)ssm_slot_stride * sb) % 16 != 0 || tile_bytes % 16 != 0)
+        return MAMBA_EALIGN;
+    CommitArgs a;
+    a.ssm_pool = ssm_pool; a.ssm_stride = ssm_slot_stride * (int64_t)sb; a.num_slots = num_slots;
+    a.conv_pool = conv_pool; a.conv_stride = conv_slot_stride;
+    a.slot = slot_ids; a.scratch = scratch_slots; a.accept = accept_len; a.ntok = ntok; a.err = err_word;
+    a.H = H; a.tile_vecs = (int)(tile_bytes / 16); a.Cd = Cd; a.Wc = Wc;
+    const size_t ab = dtype_bytes(d->conv_dtype);
+    const size_t smem = ab * (size_t)CONV_CHANNELS * Wc;
+    const int conv_units = conv_pool ? (Cd + CONV_CHANNELS - 1) / CONV_CHANNELS : 0;
+    const dim3 grid(H + conv_units, batch), block(256);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto kern = d->conv_dtype == MAMBA_BF16 ? k_spec_commit<bf16> : k_spec_commit<float>;
+    kern<<<grid, block, smem, st>>>(a);
+    return launch_status();
+}

@@ -1,0 +1,183 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* the library builds, loads and exports every function include/mamba_state.h declares;
+* the size helpers reproduce the state sizes printed on the pages (tests/golden/state_bytes.txt);
+* host-checkable argument errors return the documented status before anything is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from recurrent_state_update_gb300 import binding as bd
+from recurrent_state_update_gb300 import build as bld
+from recurrent_state_update_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba_state.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bld.build()
+    return bd.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(mamba_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("mamba_conv_update", "mamba_state_update", "mamba_chunk_scan", "mamba_spec_commit",
+              "mamba_chunk_scan_workspace_bytes", "mamba_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in bd.SIGNATURES, f"binding lacks {n}"
+
+
+def _golden():
+    out = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "state_bytes.txt")):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = (s.strip() for s in line.split("=", 1))
+            out[k] = float(v)
+    return out
+
+
+def test_state_sizes_match_the_pages(lib):
+    g = _golden()
+    f32_ssm = bd.layer_desc(wl.NEMOTRON_H_8B, state=wl.F32, act=wl.BF16)
+    bf16_ssm = bd.layer_desc(wl.NEMOTRON_H_8B, state=wl.BF16, act=wl.BF16)
+    assert bd.mamba_conv_dim(f32_ssm) == 10240
+    ssm32 = bd.mamba_ssm_state_bytes(f32_ssm)
+    ssm16 = bd.mamba_ssm_state_bytes(bf16_ssm)
+    conv = bd.mamba_conv_state_bytes(f32_ssm)
+    assert ssm16 == wl.NEMOTRON_H_8B.nheads * wl.NEMOTRON_H_8B.head_dim * wl.NEMOTRON_H_8B.d_state * 2
+    # the page's 97.4 MiB: 24 layers of fp32 SSM + bf16 conv state
+    assert 24 * (ssm32 + conv) == g["seq_state_bytes_24_layers_f32_ssm_bf16_conv"]
+    assert round((ssm32 + conv) / 2 ** 20, 2) == g["layer_state_mib_f32_ssm_bf16_conv"]
+    assert round(100 * conv / (ssm32 + conv), 1) == g["conv_share_percent"]
+    assert int(24 * (ssm32 + conv) / (128 * 1024)) == g["crossover_tokens_vs_128KiB_per_token_f32"]
+    assert int(24 * (ssm16 + conv) / (128 * 1024)) == g["crossover_tokens_vs_128KiB_per_token_bf16"]
+    # the other page's 96 MiB: 48 layers of bf16 SSM state
+    assert 48 * ssm16 == g["seq_ssm_bytes_48_layers_bf16"]
+    assert 48 * ssm16 / 2 ** 20 == g["seq_ssm_mib_48_layers_bf16"]
+    assert 48 * ssm16 / g["kv_bytes_per_token"] == g["crossover_tokens_48_layers"]
+    # speculative columns widen the conv state only
+    spec = bd.layer_desc(wl.NEMOTRON_H_8B.with_spec(4), state=wl.BF16, act=wl.BF16)
+    assert bd.mamba_conv_state_bytes(spec) == 10240 * 7 * 2
+    assert bd.mamba_ssm_state_bytes(spec) == ssm16
+
+
+def test_supported_shapes(lib):
+    assert bd.mamba_decode_supported(bd.layer_desc(wl.NEMOTRON_H_8B)) == bd.MAMBA_OK
+    assert bd.mamba_decode_supported(bd.layer_desc(wl.TINY, state=wl.F32, act=wl.F32)) == bd.MAMBA_OK
+    odd = wl.LayerShape(nheads=4, head_dim=24, d_state=40, n_groups=1)
+    assert bd.mamba_decode_supported(bd.layer_desc(odd)) == bd.MAMBA_EUNSUPPORTED
+    bad = wl.LayerShape(nheads=6, head_dim=64, d_state=128, n_groups=4)  # 6 % 4 != 0
+    assert bd.mamba_decode_supported(bd.layer_desc(bad)) == bd.MAMBA_EINVAL
+    assert bd.mamba_conv_dim(bd.layer_desc(bad)) == -1
+    mixed = bd.layer_desc(wl.NEMOTRON_H_8B, conv=wl.F32)  # conv dtype != act dtype
+    assert bd.mamba_decode_supported(mixed) == bd.MAMBA_EUNSUPPORTED
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert bd.status_string(code).startswith("MAMBA_")
+    assert "unknown" in bd.status_string(7)
+
+
+def test_workspace_bytes(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    ws = bd.mamba_chunk_scan_workspace_bytes(d, 32768, 8, 256)
+    # at least the per-chunk fp32 states of every chunk (each sequence adds <= 1 partial chunk)
+    assert ws >= (32768 // 256 + 8) * 128 * 64 * 128 * 4
+    assert bd.mamba_chunk_scan_workspace_bytes(d, -1, 8, 256) == 0
+
+
+# --------------------------------------------------------------------------------------------
+# host-side validation: every call below returns before any CUDA call is made
+# --------------------------------------------------------------------------------------------
+
+FAKE = 0x10000  # a 16-byte aligned non-null value; never dereferenced because validation fails first
+
+
+def _state_update(lib, desc, **over):
+    args = dict(ssm=FAKE, ssm_stride=128 * 64 * 128, num_slots=8, conv=None, conv_stride=0, conv_w=None,
+                conv_b=None, slot=FAKE, scratch=None, batch=4, ntok=1, xbc=FAKE, dt=FAKE, A=FAKE, D=None,
+                dt_bias=None, softplus=1, z=None, y=FAKE)
+    args.update(over)
+    return lib.mamba_state_update(ctypes.byref(desc), args["ssm"], args["ssm_stride"], args["num_slots"],
+                                  args["conv"], args["conv_stride"], args["conv_w"], args["conv_b"], args["slot"],
+                                  args["scratch"], args["batch"], args["ntok"], args["xbc"], args["dt"], args["A"],
+                                  args["D"], args["dt_bias"], args["softplus"], args["z"], args["y"], None, None)
+
+
+def test_state_update_host_errors(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    assert _state_update(lib, d, batch=0) == bd.MAMBA_OK  # nothing to do, nothing launched
+    assert _state_update(lib, d, ssm=None) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, slot=None) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, A=None) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, batch=-1) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, ntok=0) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, ntok=9) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, ssm_stride=100) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, num_slots=0) == bd.MAMBA_EINVAL
+    assert _state_update(lib, d, conv=FAKE, conv_stride=10240 * 3) == bd.MAMBA_EINVAL  # conv_w missing
+    assert _state_update(lib, d, ssm=FAKE + 8) == bd.MAMBA_EALIGN
+    assert _state_update(lib, d, ssm_stride=128 * 64 * 128 + 4) == bd.MAMBA_EALIGN
+    assert _state_update(lib, d, y=FAKE + 1) == bd.MAMBA_EALIGN
+    odd = bd.layer_desc(wl.LayerShape(nheads=4, head_dim=24, d_state=40, n_groups=1))
+    assert _state_update(lib, odd, ssm_stride=4 * 24 * 40) == bd.MAMBA_EUNSUPPORTED
+    bad = bd.LayerDesc(128, 64, 128, 8, 4, 0, 1, 1, 1, 7)  # dt dtype code 7
+    assert _state_update(lib, bad) == bd.MAMBA_EINVAL
+    assert _state_update(lib, bd.LayerDesc(128, 64, 128, 8, 9, 0, 1, 1, 1, 0)) == bd.MAMBA_EINVAL  # W > 8
+
+
+def test_conv_and_commit_host_errors(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    r = lib.mamba_conv_update(ctypes.byref(d), None, 10240 * 3, 8, FAKE, 4, 1, FAKE, FAKE, None, FAKE, None, None)
+    assert r == bd.MAMBA_EINVAL
+    r = lib.mamba_conv_update(ctypes.byref(d), FAKE, 10, 8, FAKE, 4, 1, FAKE, FAKE, None, FAKE, None, None)
+    assert r == bd.MAMBA_EINVAL
+    r = lib.mamba_conv_update(ctypes.byref(d), FAKE, 10240 * 3, 8, FAKE, 0, 1, FAKE, FAKE, None, FAKE, None, None)
+    assert r == bd.MAMBA_OK
+    # commit: ntok beyond num_spec cannot re-seat the conv window
+    r = lib.mamba_spec_commit(ctypes.byref(d), FAKE, 128 * 64 * 128, 8, FAKE, 10240 * 3, FAKE, FAKE, FAKE, 4, 4,
+                              None, None)
+    assert r == bd.MAMBA_EINVAL
+    r = lib.mamba_spec_commit(ctypes.byref(d), None, 128 * 64 * 128, 8, None, 0, FAKE, FAKE, FAKE, 4, 4, None, None)
+    assert r == bd.MAMBA_EINVAL
+
+
+def test_chunk_scan_host_errors(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    need = bd.mamba_chunk_scan_workspace_bytes(d, 1000, 2, 256)
+
+    def call(**over):
+        a = dict(ssm=FAKE, stride=128 * 64 * 128, ns=8, cu=FAKE, nseq=2, T=1000, slot=FAKE, hi=None, ck=None, mc=0,
+                 ci=0, chunk=256, x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, ws=FAKE, wsb=need)
+        a.update(over)
+        return lib.mamba_chunk_scan(ctypes.byref(d), a["ssm"], a["stride"], a["ns"], a["cu"], a["nseq"], a["T"],
+                                    a["slot"], a["hi"], a["ck"], a["mc"], a["ci"], a["chunk"], a["x"], a["dt"],
+                                    a["A"], a["B"], a["C"], None, None, 1, None, FAKE, a["ws"], a["wsb"], None, None)
+
+    assert call(nseq=0) == bd.MAMBA_OK
+    assert call(ssm=None) == bd.MAMBA_EINVAL
+    assert call(ws=None) == bd.MAMBA_EINVAL
+    assert call(wsb=need - 1) == bd.MAMBA_ENOSPACE
+    assert call(chunk=128) == bd.MAMBA_EUNSUPPORTED
+    assert call(ck=FAKE, mc=4, ci=1000) == bd.MAMBA_EINVAL  # interval not a multiple of the chunk
+    assert call(ws=FAKE + 4) == bd.MAMBA_EALIGN

@@ -1,0 +1,324 @@
+"""GPU parity of the decode path against the fp64 oracle, through the C ABI.
+
+Tolerances (max relative error per tile: (slot, head) for states, (row, head) for outputs):
+  fp32 state: 1e-4;  bf16 state: 2e-2 per step (the oracle is fed the GPU's own bf16 state from
+  before the step) and 3e-2 after 64 independent steps (oracle chain kept in fp64).
+Slot indexing, padding and every byte the call must not touch are compared exactly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from recurrent_state_update_gb300 import binding as bd
+from recurrent_state_update_gb300 import build as bld
+from recurrent_state_update_gb300 import workloads as wl
+
+from gpu_util import device_normal_pool, f64, tile_rel_err, to_dev, to_i32
+
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = 1e-4
+BF16_STEP_TOL = 2e-2
+BF16_DRIFT_TOL = 3e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    bld.build()
+    bd.lib()
+    torch.cuda.set_device(0)
+
+
+class Layer:
+    """One layer's parameters on the device and as fp64 for the oracle."""
+
+    def __init__(self, shape, seed, act=wl.BF16):
+        self.shape = shape
+        self.prm = wl.layer_params(wl.rng(seed, 0), shape)
+        self.d = {k: to_dev(v, wl.F32) for k, v in self.prm.items()}
+        self.o = {k: v.astype(np.float64) for k, v in self.prm.items()}
+        self.act = act
+
+
+def _step_inputs(layer, seed, step, batch, ntok=1, with_z=True):
+    inp = wl.decode_inputs(wl.rng(seed, 1, step), layer.shape, layer.prm, batch, ntok, layer.act, with_z)
+    dev = dict(xbc=to_dev(inp["xbc"], layer.act), dt=to_dev(inp["dt"], wl.F32), z=to_dev(inp["z"], layer.act))
+    o = dict(xbc=wl.upcast(inp["xbc"], layer.act), dt=inp["dt"].astype(np.float64),
+             z=None if inp["z"] is None else wl.upcast(inp["z"], layer.act))
+    return dev, o
+
+
+def _gpu_step(desc, layer, ssm, conv, slot_t, dev, y, scratch_t=None, err=None):
+    bd.mamba_state_update(desc, ssm, slot_t, dev["xbc"], dev["dt"], layer.d["A"], y, conv_pool=conv,
+                          conv_w=layer.d["conv_w"], scratch_slots=scratch_t, D=layer.d["D"],
+                          dt_bias=layer.d["dt_bias"], z=dev["z"], err_word=err)
+
+
+def _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=None):
+    z = None if o["z"] is None else o["z"].reshape(o["z"].shape[0], o["z"].shape[1], layer.shape.nheads, -1)
+    return oracle.decode(o_ssm, slot, o["xbc"], o["dt"], layer.o["A"], conv_pool=o_conv, conv_w=layer.o["conv_w"],
+                         scratch=scratch, D=layer.o["D"], dt_bias=layer.o["dt_bias"], z=z,
+                         n_groups=layer.shape.n_groups)
+
+
+def test_tiny_fp32_decode_32_steps():
+    """4 x 16 x 16 fp32 state, batch 4 of 8 slots, 32 sequential steps, conv fused."""
+    import torch
+    cfg = wl.TINY_DECODE
+    shape, S, batch = cfg["shape"], cfg["pool"], cfg["batch"]
+    layer = Layer(shape, cfg["seed"], act=wl.F32)
+    st = wl.initial_states(wl.rng(cfg["seed"], 2), shape, S, wl.F32, wl.F32)
+    slot = wl.slot_ids(wl.rng(cfg["seed"], 3), S, batch)
+    desc = bd.layer_desc(shape, state=wl.F32, act=wl.F32)
+    ssm, conv = to_dev(st["ssm"], wl.F32), to_dev(st["conv"], wl.F32)
+    o_ssm, o_conv = st["ssm"].astype(np.float64), st["conv"].astype(np.float64)
+    slot_t = to_i32(slot)
+    untouched = np.setdiff1d(np.arange(S), slot)
+    for step in range(cfg["steps"]):
+        dev, o = _step_inputs(layer, cfg["seed"], step, batch)
+        y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda")
+        _gpu_step(desc, layer, ssm, conv, slot_t, dev, y)
+        y_o = _oracle_step(layer, o_ssm, o_conv, slot, o)
+        assert tile_rel_err(f64(y).reshape(batch, shape.nheads, -1), y_o.reshape(batch, shape.nheads, -1), 1) < FP32_TOL
+        assert tile_rel_err(f64(ssm)[slot], o_ssm[slot], 2) < FP32_TOL
+        np.testing.assert_array_equal(f64(conv)[slot], o_conv[slot])  # conv state holds raw inputs
+    np.testing.assert_array_equal(f64(ssm)[untouched], st["ssm"][untouched].astype(np.float64))
+    np.testing.assert_array_equal(f64(conv)[untouched], st["conv"][untouched].astype(np.float64))
+
+
+def _nemotron_pools(S, seed, state=wl.BF16, spec=0):
+    shape = wl.NEMOTRON_H_8B.with_spec(spec)
+    ssm = device_normal_pool((S, shape.nheads, shape.head_dim, shape.d_state), state, seed)
+    conv = device_normal_pool((S, shape.conv_dim, shape.conv_cols), wl.BF16, seed + 1000)
+    return shape, ssm, conv
+
+
+@pytest.mark.parametrize("state", [wl.BF16, wl.F32])
+def test_nemotron_decode_batch256_one_step(state):
+    """Nemotron-H-8B layer shape, batch 256 of 512 random slots, one step, every row checked."""
+    import torch
+    S, batch, seed = 512, 256, 11
+    shape, ssm, conv = _nemotron_pools(S, seed, state)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape, state=state, act=wl.BF16)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
+    ssm0, conv0 = ssm.clone(), conv.clone()
+    sl = torch.from_numpy(slot).long().cuda()
+    # the oracle works on a compact pool holding just the batch's slots (row i -> slot i)
+    o_ssm, o_conv = f64(ssm[sl]), f64(conv[sl])
+    compact = np.arange(batch, dtype=np.int32)
+    dev, o = _step_inputs(layer, seed, 0, batch)
+    y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y)
+    torch.cuda.synchronize()
+    y_o = _oracle_step(layer, o_ssm, o_conv, compact, o)
+    tol = BF16_STEP_TOL if state == wl.BF16 else FP32_TOL
+    assert tile_rel_err(f64(ssm[sl]), o_ssm, 2) < tol
+    assert tile_rel_err(f64(y).reshape(batch, shape.nheads, -1), y_o.reshape(batch, shape.nheads, -1), 1) < 2e-2
+    np.testing.assert_array_equal(f64(conv[sl]), o_conv)
+    mask = torch.ones(S, dtype=torch.bool, device="cuda")
+    mask[sl] = False
+    assert torch.equal(ssm[mask], ssm0[mask])
+    assert torch.equal(conv[mask], conv0[mask])
+
+
+@pytest.mark.parametrize("batch", [1, 8, 64, 256, 1024])
+def test_padding_sweep_16_steps(batch):
+    """1536-slot pool, 10% of rows padded with -1, 16 steps; after every step the sampled rows
+    match one oracle step from the GPU's own pre-step state, padded rows' outputs and every
+    slot outside the batch are untouched."""
+    import torch
+    S, seed = 1536, 20 + batch
+    shape, ssm, conv = _nemotron_pools(S, seed)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch, 0.1)
+    live = np.flatnonzero(slot >= 0)
+    sample = live if len(live) <= 12 else np.sort(wl.rng(seed, 4).choice(live, 12, replace=False))
+    ssm0, conv0 = ssm.clone(), conv.clone()
+    mask = torch.ones(S, dtype=torch.bool, device="cuda")
+    mask[torch.from_numpy(slot[live]).long().cuda()] = False
+    slot_t = to_i32(slot)
+    sl_s = torch.from_numpy(slot[sample]).long().cuda()
+    for step in range(16):
+        dev, o = _step_inputs(layer, seed, step, batch)
+        pre_ssm, pre_conv = f64(ssm[sl_s]), f64(conv[sl_s])
+        y = torch.full((batch, 1, shape.nheads * shape.head_dim), 0x7FC1, device="cuda",
+                       dtype=torch.int16).view(torch.bfloat16)  # a NaN pattern the kernel never writes
+        _gpu_step(desc, layer, ssm, conv, slot_t, dev, y)
+        torch.cuda.synchronize()
+        # oracle on the sampled rows only, from the GPU's pre-step state
+        n = len(sample)
+        o_ssm, o_conv = pre_ssm.copy(), pre_conv.copy()
+        o_sub = dict(xbc=o["xbc"][sample], dt=o["dt"][sample], z=o["z"][sample])
+        y_o = _oracle_step(layer, o_ssm, o_conv, np.arange(n, dtype=np.int32), o_sub)
+        assert tile_rel_err(f64(ssm[sl_s]), o_ssm, 2) < BF16_STEP_TOL
+        assert tile_rel_err(f64(y[torch.from_numpy(sample).long().cuda()]).reshape(n, shape.nheads, -1),
+                            y_o.reshape(n, shape.nheads, -1), 1) < 2e-2
+        np.testing.assert_array_equal(f64(conv[sl_s]), o_conv)
+        pads = np.flatnonzero(slot < 0)
+        if len(pads):
+            yp = y[torch.from_numpy(pads).long().cuda()].view(torch.int16)
+            assert bool((yp == 0x7FC1).all())
+        assert torch.equal(ssm[mask], ssm0[mask])
+        assert torch.equal(conv[mask], conv0[mask])
+
+
+def test_bf16_drift_64_steps():
+    """64 steps with both chains independent (oracle kept in fp64): within 3e-2."""
+    import torch
+    S, batch, seed = 16, 8, 30
+    shape, ssm, conv = _nemotron_pools(S, seed)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
+    o_ssm, o_conv = f64(ssm), f64(conv)
+    slot_t = to_i32(slot)
+    sl = torch.from_numpy(slot).long().cuda()
+    for step in range(64):
+        dev, o = _step_inputs(layer, seed, step, batch)
+        y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+        _gpu_step(desc, layer, ssm, conv, slot_t, dev, y)
+        y_o = _oracle_step(layer, o_ssm, o_conv, slot, o)
+    torch.cuda.synchronize()
+    assert tile_rel_err(f64(ssm[sl]), o_ssm[slot], 2) < BF16_DRIFT_TOL
+    assert tile_rel_err(f64(y).reshape(batch, shape.nheads, -1), y_o.reshape(batch, shape.nheads, -1), 1) < BF16_DRIFT_TOL
+
+
+def test_permuted_slots_permute_results_bit_exactly():
+    import torch
+    S, batch, seed = 64, 32, 40
+    shape, ssm_a, conv_a = _nemotron_pools(S, seed)
+    ssm_b, conv_b = ssm_a.clone(), conv_a.clone()
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
+    perm = wl.rng(seed, 5).permutation(batch)
+    dev, _ = _step_inputs(layer, seed, 0, batch)
+    ya = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    yb = torch.empty_like(ya)
+    _gpu_step(desc, layer, ssm_a, conv_a, to_i32(slot), dev, ya)
+    pt = torch.from_numpy(perm).long().cuda()
+    dev_p = {k: (None if v is None else v[pt].contiguous()) for k, v in dev.items()}
+    _gpu_step(desc, layer, ssm_b, conv_b, to_i32(slot[perm]), dev_p, yb)
+    assert torch.equal(yb, ya[pt])
+    assert torch.equal(ssm_a, ssm_b)
+    assert torch.equal(conv_a, conv_b)
+
+
+def test_decode_without_conv_and_without_gate():
+    """conv_pool NULL: xbc is taken as already convolved; z NULL: no gate."""
+    import torch
+    S, batch, seed = 32, 16, 50
+    shape, ssm, _ = _nemotron_pools(S, seed)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch, 0.1)
+    o_ssm = f64(ssm)
+    dev, o = _step_inputs(layer, seed, 0, batch, with_z=False)
+    y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    bd.mamba_state_update(desc, ssm, to_i32(slot), dev["xbc"], dev["dt"], layer.d["A"], y, D=layer.d["D"],
+                          dt_bias=layer.d["dt_bias"])
+    y_o = oracle.decode(o_ssm, slot, o["xbc"], o["dt"], layer.o["A"], D=layer.o["D"], dt_bias=layer.o["dt_bias"],
+                        n_groups=shape.n_groups)
+    live = slot >= 0
+    sl = torch.from_numpy(slot[live]).long().cuda()
+    assert tile_rel_err(f64(ssm[sl]), o_ssm[slot[live]], 2) < BF16_STEP_TOL
+    yl = f64(y[torch.from_numpy(np.flatnonzero(live)).long().cuda()]).reshape(int(live.sum()), shape.nheads, -1)
+    assert tile_rel_err(yl, y_o[live].reshape(int(live.sum()), shape.nheads, -1), 1) < 2e-2
+
+
+def test_conv_update_standalone():
+    import torch
+    S, batch, seed, ntok = 24, 10, 60, 3
+    shape = wl.NEMOTRON_H_8B.with_spec(2)
+    conv = device_normal_pool((S, shape.conv_dim, shape.conv_cols), wl.BF16, seed)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch, 0.2)
+    o_conv = f64(conv)
+    dev, o = _step_inputs(layer, seed, 0, batch, ntok=ntok)
+    out = torch.zeros(batch, ntok, shape.conv_dim, device="cuda", dtype=torch.bfloat16)
+    bd.mamba_conv_update(desc, conv, to_i32(slot), dev["xbc"], layer.d["conv_w"], out)
+    torch.cuda.synchronize()
+    got = f64(conv)
+    for i, s in enumerate(slot):
+        if s < 0:
+            assert bool((out[i] == 0).all())
+            continue
+        st, ref = oracle.conv_update(o_conv[s], o["xbc"][i], layer.o["conv_w"])
+        np.testing.assert_array_equal(got[s], st)
+        g = f64(out[i])
+        assert np.abs(g - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-6
+    dead = np.setdiff1d(np.arange(S), slot)
+    np.testing.assert_array_equal(got[dead], o_conv[dead])
+
+
+def test_speculative_decode_and_commit():
+    """Batch 128, 4 draft tokens, conv state W-1+4 columns, 4 scratch slots per request, then a
+    commit of random accept lengths in 0..4."""
+    import torch
+    cfg = wl.SPEC_DECODE
+    batch, K, seed = cfg["batch"], cfg["ntok"], cfg["seed"]
+    S = batch * (1 + K) + 64
+    shape, ssm, conv = _nemotron_pools(S, seed, spec=K)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    ids = wl.rng(seed, 3).choice(S, size=batch * (1 + K), replace=False).astype(np.int32)
+    slot, scratch = ids[:batch], ids[batch:].reshape(batch, K)
+    o_ssm, o_conv = f64(ssm), f64(conv)
+    dev, o = _step_inputs(layer, seed, 0, batch, ntok=K)
+    y = torch.empty(batch, K, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    ssm0 = ssm.clone()
+    _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, scratch_t=to_i32(scratch))
+    torch.cuda.synchronize()
+    y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
+    sl = torch.from_numpy(slot).long().cuda()
+    assert torch.equal(ssm[sl], ssm0[sl])  # main slots untouched
+    for j in range(K):
+        sj = torch.from_numpy(scratch[:, j].copy()).long().cuda()
+        assert tile_rel_err(f64(ssm[sj]), o_ssm[scratch[:, j]], 2) < BF16_STEP_TOL
+        assert tile_rel_err(f64(y[:, j]).reshape(batch, shape.nheads, -1), y_o[:, j].reshape(batch, shape.nheads, -1),
+                            1) < 2e-2
+    np.testing.assert_array_equal(f64(conv[sl]), o_conv[slot])
+    # commit: exact copy and exact conv re-seat, checked against the oracle's commit applied to
+    # the GPU's own post-step pools
+    accept = wl.accept_lengths(wl.rng(seed, 6), batch, K)
+    e_ssm, e_conv = f64(ssm), f64(conv)
+    oracle.spec_commit(e_ssm, slot, scratch, accept, conv_pool=e_conv)
+    bd.mamba_spec_commit(desc, ssm, to_i32(slot), to_i32(scratch), to_i32(accept), conv_pool=conv)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(ssm), e_ssm)
+    np.testing.assert_array_equal(f64(conv), e_conv)
+
+
+def test_device_side_errors_leave_rows_untouched():
+    import torch
+    S, batch, seed = 16, 4, 70
+    shape, ssm, conv = _nemotron_pools(S, seed, spec=2)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = np.array([3, S + 5, 7, -1], np.int32)  # row 1 is out of range
+    ssm0, conv0 = ssm.clone(), conv.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev, _ = _step_inputs(layer, seed, 0, batch)
+    y = torch.zeros(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
+    assert bool((y[1] == 0).all()) and bool((y[3] == 0).all())
+    for s in range(S):
+        if s not in (3, 7):
+            assert torch.equal(ssm[s], ssm0[s]) and torch.equal(conv[s], conv0[s])
+    # commit with an accept length out of range: flagged, row untouched
+    err.zero_()
+    scratch = np.array([[8, 9], [10, 11], [12, 13], [14, 15]], np.int32)
+    accept = np.array([5, 1, 0, 2], np.int32)
+    ok_slot = np.array([3, 4, 7, -1], np.int32)
+    ssm1, conv1 = ssm.clone(), conv.clone()
+    bd.mamba_spec_commit(desc, ssm, to_i32(ok_slot), to_i32(scratch), to_i32(accept), conv_pool=conv, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.MAMBA_ERR_ACCEPT_RANGE
+    assert torch.equal(ssm[3], ssm1[3]) and torch.equal(conv[3], conv1[3])
+    assert torch.equal(ssm[4], ssm1[10])
