@@ -334,7 +334,8 @@ def run_gpu(args):
     bld.build()
     hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
 
-    dec = DecodeWorkload(torch, rank, DECODE["layers"], DECODE["batch"], DECODE["pool"])
+    layers = args.layers or DECODE["layers"]
+    dec = DecodeWorkload(torch, rank, layers, DECODE["batch"], DECODE["pool"])
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
         dec.step()
@@ -346,17 +347,34 @@ def run_gpu(args):
     ms = _max_over_ranks(torch, dist, ms)
     total_bytes = dec.bytes_per_step() * world
     value = total_bytes / (ms * 1e-3) / 1e9
-    token_layers = DECODE["layers"] * DECODE["batch"] * world / (ms * 1e-3)
+    token_layers = layers * DECODE["batch"] * world / (ms * 1e-3)
     launch_ms = ms / dec.launches_per_step
     achieved = DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER / (launch_ms * 1e-3) / 1e9
 
     # end to end: pinned host inputs in, every layer's y out, inside the timed region
-    ms_e2e = _max_over_ranks(torch, dist, _time(torch, dec.step_e2e, args.steps, 2, dist))
-    e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
-           "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
+    e2e = None
+    if args.only == "all":
+        ms_e2e = _max_over_ranks(torch, dist, _time(torch, dec.step_e2e, args.steps, 2, dist))
+        e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
     del dec
     torch.cuda.empty_cache()
+    prefill = None
+    if args.only == "all":
+        prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
 
+    cpu = None
+    if rank == 0 and world == 1 and args.only == "all" and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode()
+
+    if rank == 0:
+        emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck,
+             prefill, cpu)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
     pre = PrefillWorkload(torch, rank)
     ms_pre = _max_over_ranks(torch, dist, _time(torch, pre.step, args.steps, max(args.warmup, 3), dist))
     fl = prefill_flops(pre.lengths, PREFILL["chunk"])
@@ -371,18 +389,18 @@ def run_gpu(args):
     }
     del pre
     torch.cuda.empty_cache()
+    return prefill
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_decode()
 
-    if rank == 0:
+def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
+         cpu):
+    if True:
         line = {
             "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
-            "config": {"workload": DECODE["name"], "layers": DECODE["layers"], "global_batch": DECODE["batch"] * world,
+            "config": {"workload": DECODE["name"], "layers": layers, "global_batch": DECODE["batch"] * world,
                        "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
                        "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
                        "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"},
@@ -393,14 +411,12 @@ def run_gpu(args):
                          "algorithmic_bytes_per_launch": DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER,
                          "avg_launch_ms": launch_ms},
             "e2e": e2e,
-            "gpu_launches": args.steps * DECODE["layers"],
+            "gpu_launches": args.steps * layers,
             "clocks": ck,
             "prefill": prefill,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
 
 
 # ------------------------------------------------------------------------------------------
@@ -461,6 +477,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--layers", type=int, default=0, help="decode layers per step (default: the workload's 48)")
+    ap.add_argument("--only", choices=["all", "decode"], default="all",
+                    help="'decode' times the decode step alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -53,3 +53,14 @@ def device_normal_pool(shape, dtype, seed, std=0.1, device="cuda"):
         blk = torch.randn(flat[s0:s0 + 64].shape, generator=g, device=device, dtype=torch.float32)
         flat[s0:s0 + 64].copy_(blk.mul_(std))
     return t
+
+
+def tile_rms_err(got, ref, tile_axes):
+    """max over tiles of ||got-ref||_2 / ||ref||_2 (tile = the trailing ``tile_axes`` axes)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    axes = tuple(range(got.ndim - tile_axes, got.ndim))
+    num = np.sqrt(((got - ref) ** 2).sum(axis=axes))
+    den = np.sqrt((ref ** 2).sum(axis=axes))
+    den = np.where(den == 0, 1.0, den)
+    return float((num / den).max())

@@ -1,8 +1,9 @@
 """GPU parity of the decode path against the fp64 oracle, through the C ABI.
 
-Tolerances (max relative error per tile: (slot, head) for states, (row, head) for outputs):
-  fp32 state: 1e-4;  bf16 state: 2e-2 per step (the oracle is fed the GPU's own bf16 state from
-  before the step) and 3e-2 after 64 independent steps (oracle chain kept in fp64).
+Tolerances (relative error per tile: (slot, head) for states, (row, head) for outputs):
+  fp32 state: max error 1e-4;  bf16 state: max error 2e-2 per step (the oracle is fed the GPU's own
+  bf16 state from before the step); drift after 64 independent steps (oracle chain kept in fp64):
+  RMS error 3e-2, and max error under 64 * 2^-9, the bound for 64 round-to-nearest bf16 stores.
 Slot indexing, padding and every byte the call must not touch are compared exactly.
 """
 import numpy as np
@@ -13,7 +14,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import device_normal_pool, f64, tile_rel_err, to_dev, to_i32
+from gpu_util import device_normal_pool, f64, tile_rel_err, tile_rms_err, to_dev, to_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -166,7 +167,9 @@ def test_padding_sweep_16_steps(batch):
 
 
 def test_bf16_drift_64_steps():
-    """64 steps with both chains independent (oracle kept in fp64): within 3e-2."""
+    """64 steps with both chains independent (oracle kept in fp64).  Each step stores the state
+    in bf16 (relative rounding <= 2^-9), so the deviation of single elements grows like a random
+    walk; the drift bound applies to the RMS error per tile, the max error to the worst case."""
     import torch
     S, batch, seed = 16, 8, 30
     shape, ssm, conv = _nemotron_pools(S, seed)
@@ -182,8 +185,13 @@ def test_bf16_drift_64_steps():
         _gpu_step(desc, layer, ssm, conv, slot_t, dev, y)
         y_o = _oracle_step(layer, o_ssm, o_conv, slot, o)
     torch.cuda.synchronize()
-    assert tile_rel_err(f64(ssm[sl]), o_ssm[slot], 2) < BF16_DRIFT_TOL
-    assert tile_rel_err(f64(y).reshape(batch, shape.nheads, -1), y_o.reshape(batch, shape.nheads, -1), 1) < BF16_DRIFT_TOL
+    got_h = f64(ssm[sl])
+    got_y = f64(y).reshape(batch, shape.nheads, -1)
+    ref_y = y_o.reshape(batch, shape.nheads, -1)
+    assert tile_rms_err(got_h, o_ssm[slot], 2) < BF16_DRIFT_TOL
+    assert tile_rms_err(got_y, ref_y, 1) < BF16_DRIFT_TOL
+    assert tile_rel_err(got_h, o_ssm[slot], 2) < 64 * 2.0 ** -9
+    assert tile_rel_err(got_y, ref_y, 1) < 64 * 2.0 ** -9
 
 
 def test_permuted_slots_permute_results_bit_exactly():
