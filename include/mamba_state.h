@@ -230,6 +230,40 @@ int mamba_chunk_scan(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_s
                      const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
                      void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream);
 
+/* ---------------------------------------------------------------------------------------- */
+/* chunked prefill without a caller workspace                                               */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * mamba_chunk_scan_noalloc -- the same operation, arguments and results as mamba_chunk_scan,
+ * for callers that cannot provide a device workspace.  The pages have no counterpart: this
+ * entry point exists for callers that must not allocate device memory, such as an engine whose
+ * memory pool has already reserved the GPU (a further cudaMalloc fails, or synchronises the
+ * whole device and stalls every stream) or a latency-critical path that may not call
+ * cudaMalloc / cudaFree.  It allocates nothing and calls no allocating routine.
+ *
+ * Its scratch is one fixed array of mamba_chunk_scan_static_scratch_bytes() bytes (128 MiB)
+ * compiled into the library: every GPU that loads the library holds that memory until the
+ * process exits.  A call whose workspace would exceed it (mamba_chunk_scan_workspace_bytes
+ * larger than that size) returns MAMBA_ENOSPACE and launches nothing.
+ *
+ * The first call on each device looks up that device's address of the array (with the device
+ * current); make that first call before any stream capture.  All calls share the one array and
+ * nothing in it carries over between calls, but two calls that run at the same time on the GPU
+ * (on different streams or from different host threads) race on it: order them.
+ */
+int mamba_chunk_scan_noalloc(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                             int64_t num_slots, const int32_t *cu_seqlens, int32_t nseq,
+                             int32_t total_tokens, const int32_t *slot_ids,
+                             const uint8_t *has_initial_state, const int32_t *ckpt_slots,
+                             int32_t max_ckpt, int32_t ckpt_interval, int32_t chunk, const void *x,
+                             const void *dt, const float *A, const void *B, const void *C,
+                             const float *D, const float *dt_bias, int32_t dt_softplus, const void *z,
+                             void *y, int32_t *err_word, void *stream);
+
+/* Size in bytes of the fixed scratch mamba_chunk_scan_noalloc uses (no counterpart on the pages). */
+size_t mamba_chunk_scan_static_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

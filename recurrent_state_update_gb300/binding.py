@@ -64,6 +64,9 @@ SIGNATURES = {
     "mamba_chunk_scan_workspace_bytes": (_sz, [_dp, _i32, _i32, _i32]),
     "mamba_chunk_scan": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "mamba_chunk_scan_noalloc": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32,
+                                                _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "mamba_chunk_scan_static_scratch_bytes": (_sz, []),
 }
 
 
@@ -195,3 +198,23 @@ def mamba_chunk_scan(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x, dt, A, 
                                 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                 _ptr(err_word), _stream(stream))
     _check(rc, "mamba_chunk_scan")
+
+
+def mamba_chunk_scan_static_scratch_bytes() -> int:
+    return lib().mamba_chunk_scan_static_scratch_bytes()
+
+
+def mamba_chunk_scan_noalloc(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x, dt, A, B, C, y, *,
+                             has_initial_state=None, ckpt_slots=None, ckpt_interval=0, chunk=256, D=None,
+                             dt_bias=None, dt_softplus=True, z=None, err_word=None, stream=None):
+    """mamba_chunk_scan for callers that cannot allocate: the library's fixed scratch is used
+    instead of a caller workspace (see the C header for its size limit and sharing rules)."""
+    nseq = int(cu_seqlens.shape[0]) - 1
+    total = int(x.shape[0])
+    max_ckpt = int(ckpt_slots.shape[1]) if ckpt_slots is not None else 0
+    rc = lib().mamba_chunk_scan_noalloc(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                                        _cptr(cu_seqlens), nseq, total, _cptr(slot_ids), _cptr(has_initial_state),
+                                        _cptr(ckpt_slots), max_ckpt, int(ckpt_interval), int(chunk), _cptr(x),
+                                        _cptr(dt), _cptr(A), _cptr(B), _cptr(C), _cptr(D), _cptr(dt_bias),
+                                        int(bool(dt_softplus)), _cptr(z), _cptr(y), _ptr(err_word), _stream(stream))
+    _check(rc, "mamba_chunk_scan_noalloc")

@@ -12,6 +12,8 @@
 //
 // This file is the portable CUDA-core form: six launches that communicate through a
 // caller-provided workspace (chunk table, Delta and cum, G per group, per-chunk states).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ms {
@@ -438,6 +440,93 @@ extern "C" int mamba_chunk_scan(const mamba_layer_desc *d, void *ssm_pool, int64
     const ScanLayout L = scan_layout(total_tokens, nseq, chunk, H, G, P, N);
     if (workspace_bytes < L.total) return MAMBA_ENOSPACE;
     if (!aligned16(workspace) || !aligned16(ssm_pool)) return MAMBA_EALIGN;
+    ScanArgs a;
+    a.ssm_pool = ssm_pool; a.ssm_stride = ssm_slot_stride; a.num_slots = num_slots;
+    a.cu = cu_seqlens; a.slot = slot_ids; a.has_init = has_initial_state;
+    a.ckpt_slots = ckpt_slots; a.max_ckpt = ckpt_slots ? max_ckpt : 0; a.ckpt_interval = ckpt_interval;
+    a.nseq = nseq; a.T = total_tokens; a.Q = chunk; a.H = H; a.G = G; a.HG = H / G; a.P = P; a.N = N;
+    a.x = x; a.dt = dt; a.B = B; a.C = C; a.z = z; a.dt_bf16 = d->dt_dtype == MAMBA_BF16;
+    a.dt_softplus = dt_softplus != 0; a.A = A; a.D = D; a.dt_bias = dt_bias; a.y = y; a.err = err_word;
+    a.nchunks_max = L.nchunks_max;
+    char *ws = static_cast<char *>(workspace);
+    a.meta = reinterpret_cast<int32_t *>(ws + L.off_meta);
+    a.dl = reinterpret_cast<float *>(ws + L.off_dl);
+    a.cum = reinterpret_cast<float *>(ws + L.off_cum);
+    a.cb = reinterpret_cast<float *>(ws + L.off_cb);
+    a.states = reinterpret_cast<float *>(ws + L.off_states);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool abf = d->act_dtype == MAMBA_BF16, sbf = d->state_dtype == MAMBA_BF16;
+    if (abf && sbf) return launch_scan<bf16, bf16>(a, st);
+    if (abf && !sbf) return launch_scan<bf16, float>(a, st);
+    if (!abf && sbf) return launch_scan<float, bf16>(a, st);
+    return launch_scan<float, float>(a, st);
+}
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free variant of mamba_chunk_scan.
+//
+// Some callers cannot hand this library a workspace: an engine that reserves all device
+// memory for its own pool up front (a further cudaMalloc fails or forces a device-wide
+// synchronisation that stalls every stream), or a latency-critical path that must not call
+// cudaMalloc / cudaFree at all.  For them the scratch lives in one file-scope device array
+// of fixed size.  Every GPU that loads this library holds that array until the process
+// exits.  All calls share it: two calls that overlap on the GPU (different streams, or
+// different host threads) race on it, so callers must order them.  Nothing in it needs to
+// start at zero (each launch writes what it reads), so it is not cleared between calls.
+// ---------------------------------------------------------------------------------------
+
+#define MS_STATIC_SCAN_SCRATCH_BYTES (128ull << 20)
+
+static __device__ __align__(256) unsigned char g_scan_scratch[MS_STATIC_SCAN_SCRATCH_BYTES];
+
+// Per-device address of g_scan_scratch, looked up once per device (with that device current).
+static void *static_scratch_address(int *status) {
+    constexpr int kMaxDevices = 64;
+    static void *addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *status = MAMBA_ECUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess || !p) {
+            *status = MAMBA_ECUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    *status = MAMBA_OK;
+    return addr[dev];
+}
+
+extern "C" size_t mamba_chunk_scan_static_scratch_bytes(void) { return MS_STATIC_SCAN_SCRATCH_BYTES; }
+
+extern "C" int mamba_chunk_scan_noalloc(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride,
+                                        int64_t num_slots, const int32_t *cu_seqlens, int32_t nseq,
+                                        int32_t total_tokens, const int32_t *slot_ids,
+                                        const uint8_t *has_initial_state, const int32_t *ckpt_slots,
+                                        int32_t max_ckpt, int32_t ckpt_interval, int32_t chunk, const void *x,
+                                        const void *dt, const float *A, const void *B, const void *C,
+                                        const float *D, const float *dt_bias, int32_t dt_softplus, const void *z,
+                                        void *y, int32_t *err_word, void *stream) {
+    int rc = check_desc(d);
+    if (rc != MAMBA_OK) return rc;
+    if (nseq < 0 || total_tokens < 0 || chunk <= 0) return MAMBA_EINVAL;
+    if (nseq == 0) return MAMBA_OK;
+    if (!ssm_pool || !cu_seqlens || !slot_ids || !A) return MAMBA_EINVAL;
+    if (total_tokens > 0 && (!x || !dt || !B || !C || !y)) return MAMBA_EINVAL;
+    const int H = d->nheads, P = d->head_dim, N = d->d_state, G = d->n_groups;
+    if (num_slots <= 0 || ssm_slot_stride < (int64_t)H * P * N) return MAMBA_EINVAL;
+    if (ckpt_slots && (max_ckpt <= 0 || ckpt_interval <= 0 || ckpt_interval % chunk)) return MAMBA_EINVAL;
+    if ((rc = scan_shape_ok(d, chunk)) != MAMBA_OK) return rc;
+    const ScanLayout L = scan_layout(total_tokens, nseq, chunk, H, G, P, N);
+    if (L.total > MS_STATIC_SCAN_SCRATCH_BYTES) return MAMBA_ENOSPACE;  // problem too large for the fixed scratch
+    if (!aligned16(ssm_pool)) return MAMBA_EALIGN;
+    void *workspace = static_scratch_address(&rc);
+    if (rc != MAMBA_OK) return rc;
     ScanArgs a;
     a.ssm_pool = ssm_pool; a.ssm_stride = ssm_slot_stride; a.num_slots = num_slots;
     a.cu = cu_seqlens; a.slot = slot_ids; a.has_init = has_initial_state;
