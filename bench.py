@@ -334,6 +334,13 @@ def run_gpu(args):
     bld.build()
     hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
 
+    if args.only == "prefill":
+        prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
+        if rank == 0:
+            print(json.dumps({"prefill": prefill}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     layers = args.layers or DECODE["layers"]
     dec = DecodeWorkload(torch, rank, layers, DECODE["batch"], DECODE["pool"])
     clocks = ClockSampler(local)
@@ -385,7 +392,8 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
         "hbm_frac": by / (ms_pre * 1e-3) / 1e9 / hbm_peak,
         "tensor_frac": fl / (ms_pre * 1e-3) / 1e12 / bf16_peak,
         "algorithmic_bytes": by, "algorithmic_flops": fl,
-        "launches_per_layer": 6,
+        "launches_per_layer": 2,
+        "kernel": "k_ssd_tc (tcgen05) after k_tc_meta",
     }
     del pre
     torch.cuda.empty_cache()
@@ -478,8 +486,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--layers", type=int, default=0, help="decode layers per step (default: the workload's 48)")
-    ap.add_argument("--only", choices=["all", "decode"], default="all",
-                    help="'decode' times the decode step alone (profiling runs)")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="'decode' or 'prefill' times that form alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

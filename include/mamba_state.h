@@ -63,6 +63,8 @@ typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
 #define MAMBA_ERR_SLOT_RANGE 0x1   /* a slot / scratch / checkpoint slot id outside [0, num_slots) */
 #define MAMBA_ERR_ACCEPT_RANGE 0x2 /* an accept length outside [0, ntok] */
 #define MAMBA_ERR_SEQLENS 0x4      /* cu_seqlens not non-decreasing from 0 to total_tokens */
+#define MAMBA_ERR_TIMEOUT 0x8      /* an asynchronous copy or matrix operation did not complete within the
+                                      kernel's bounded wait; that row / sequence is incomplete */
 
 /* One Mamba2 layer [P1 state shapes, P4 block equations]. */
 typedef struct mamba_layer_desc {

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libmamba_state.so")
 
 MAMBA_OK, MAMBA_EINVAL, MAMBA_EUNSUPPORTED, MAMBA_ECUDA, MAMBA_EALIGN, MAMBA_ENOSPACE = 0, -1, -2, -3, -4, -5
 MAMBA_F32, MAMBA_BF16 = 0, 1
-MAMBA_ERR_SLOT_RANGE, MAMBA_ERR_ACCEPT_RANGE, MAMBA_ERR_SEQLENS = 0x1, 0x2, 0x4
+MAMBA_ERR_SLOT_RANGE, MAMBA_ERR_ACCEPT_RANGE, MAMBA_ERR_SEQLENS, MAMBA_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 
 class MambaError(RuntimeError):

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "scan_tc.h"
 
 namespace ms {
 
@@ -414,9 +415,35 @@ static int scan_shape_ok(const mamba_layer_desc *d, int chunk) {
     return MAMBA_OK;
 }
 
+// The tensor-core path (bf16 activations, head_dim 64, d_state 128): returns a status, or 1 when
+// the layer is not eligible and the portable path must run.
+static int try_scan_tc(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride, int64_t num_slots,
+                       const int32_t *cu_seqlens, int32_t nseq, int32_t total_tokens, const int32_t *slot_ids,
+                       const uint8_t *has_initial_state, const int32_t *ckpt_slots, int32_t max_ckpt,
+                       int32_t ckpt_interval, int32_t chunk, const void *x, const void *dt, const float *A,
+                       const void *B, const void *C, const float *D, const float *dt_bias, int32_t dt_softplus,
+                       const void *z, void *y, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                       cudaStream_t st) {
+    if (!scan_tc_eligible(d, chunk)) return 1;
+    if (workspace_bytes < scan_tc_workspace_bytes(nseq)) return MAMBA_ENOSPACE;
+    if (!aligned16(workspace) || !aligned16(ssm_pool) || !aligned16(x) || !aligned16(B) || !aligned16(C) ||
+        !aligned16(y) || (z && !aligned16(z)))
+        return MAMBA_EALIGN;
+    ScanTcParams p;
+    p.ssm_pool = ssm_pool; p.ssm_stride = ssm_slot_stride; p.num_slots = num_slots;
+    p.cu = cu_seqlens; p.slot = slot_ids; p.has_init = has_initial_state;
+    p.ckpt_slots = ckpt_slots; p.max_ckpt = ckpt_slots ? max_ckpt : 0; p.ckpt_interval = ckpt_interval;
+    p.nseq = nseq; p.T = total_tokens; p.H = d->nheads; p.G = d->n_groups; p.HG = d->nheads / d->n_groups;
+    p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z; p.dt_bf16 = d->dt_dtype == MAMBA_BF16;
+    p.dt_softplus = dt_softplus != 0; p.A = A; p.D = D; p.dt_bias = dt_bias; p.y = y; p.err = err_word;
+    p.meta = static_cast<int32_t *>(workspace);
+    return scan_tc_launch(p, d->state_dtype == MAMBA_BF16, st);
+}
+
 extern "C" size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *d, int32_t total_tokens, int32_t nseq,
                                                    int32_t chunk) {
     if (check_desc(d) != MAMBA_OK || total_tokens < 0 || nseq < 0 || chunk <= 0) return 0;
+    if (scan_tc_eligible(d, chunk)) return scan_tc_workspace_bytes(nseq);
     return scan_layout(total_tokens, nseq, chunk, d->nheads, d->n_groups, d->head_dim, d->d_state).total;
 }
 
@@ -436,6 +463,10 @@ extern "C" int mamba_chunk_scan(const mamba_layer_desc *d, void *ssm_pool, int64
     const int H = d->nheads, P = d->head_dim, N = d->d_state, G = d->n_groups;
     if (num_slots <= 0 || ssm_slot_stride < (int64_t)H * P * N) return MAMBA_EINVAL;
     if (ckpt_slots && (max_ckpt <= 0 || ckpt_interval <= 0 || ckpt_interval % chunk)) return MAMBA_EINVAL;
+    rc = try_scan_tc(d, ssm_pool, ssm_slot_stride, num_slots, cu_seqlens, nseq, total_tokens, slot_ids,
+                     has_initial_state, ckpt_slots, max_ckpt, ckpt_interval, chunk, x, dt, A, B, C, D, dt_bias,
+                     dt_softplus, z, y, workspace, workspace_bytes, err_word, static_cast<cudaStream_t>(stream));
+    if (rc != 1) return rc;
     if ((rc = scan_shape_ok(d, chunk)) != MAMBA_OK) return rc;
     const ScanLayout L = scan_layout(total_tokens, nseq, chunk, H, G, P, N);
     if (workspace_bytes < L.total) return MAMBA_ENOSPACE;
@@ -521,6 +552,15 @@ extern "C" int mamba_chunk_scan_noalloc(const mamba_layer_desc *d, void *ssm_poo
     const int H = d->nheads, P = d->head_dim, N = d->d_state, G = d->n_groups;
     if (num_slots <= 0 || ssm_slot_stride < (int64_t)H * P * N) return MAMBA_EINVAL;
     if (ckpt_slots && (max_ckpt <= 0 || ckpt_interval <= 0 || ckpt_interval % chunk)) return MAMBA_EINVAL;
+    if (scan_tc_eligible(d, chunk)) {
+        if (scan_tc_workspace_bytes(nseq) > MS_STATIC_SCAN_SCRATCH_BYTES) return MAMBA_ENOSPACE;
+        void *ws = static_scratch_address(&rc);
+        if (rc != MAMBA_OK) return rc;
+        return try_scan_tc(d, ssm_pool, ssm_slot_stride, num_slots, cu_seqlens, nseq, total_tokens, slot_ids,
+                           has_initial_state, ckpt_slots, max_ckpt, ckpt_interval, chunk, x, dt, A, B, C, D,
+                           dt_bias, dt_softplus, z, y, ws, MS_STATIC_SCAN_SCRATCH_BYTES, err_word,
+                           static_cast<cudaStream_t>(stream));
+    }
     if ((rc = scan_shape_ok(d, chunk)) != MAMBA_OK) return rc;
     const ScanLayout L = scan_layout(total_tokens, nseq, chunk, H, G, P, N);
     if (L.total > MS_STATIC_SCAN_SCRATCH_BYTES) return MAMBA_ENOSPACE;  // problem too large for the fixed scratch

@@ -22,6 +22,7 @@
 //  - The first head's state loads are issued before the conv phase so they are in flight
 //    while the CTA convolves.
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace ms {
 
@@ -156,20 +157,33 @@ struct DecodeArgs {
     void *y;
     int32_t *err;
     int H, G, HG, W, Wc, Cd;
+    int sps;  // state-tile stages per head slot
 };
 
-// Shared-memory floats the decode kernel needs (the conv staging area follows, in ActT).
+// Bound on the polls of one mbarrier wait (a copy that never lands is reported, not waited on forever).
+constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr int kFlagWords = 16;
+
+// Shared-memory floats after the tile stages, barriers and flags (the conv staging area follows, in ActT).
 __host__ __device__ inline int decode_smem_floats(int ntok, int LC, int HG, int P, bool conv) {
     return ntok * LC + (conv ? ntok * LC : 0) + 2 * ntok * HG + ntok * HG * P;
 }
 
-template <typename StateT, int P, int N>
-__device__ __forceinline__ void load_tile(uint4 (&raw)[Tile<StateT, P, N>::PASSES], const StateT *base,
-                                          int th) {
-    using TL = Tile<StateT, P, N>;
-#pragma unroll
-    for (int pass = 0; pass < TL::PASSES; ++pass)
-        raw[pass] = __ldcs(reinterpret_cast<const uint4 *>(base) + pass * TL::TH + th);
+// Byte offset of the float area: after S tile stages and S mbarriers (padded to 16 bytes) and the flags.
+__host__ __device__ inline size_t decode_float_offset(int S, size_t tile_bytes) {
+    return (size_t)S * tile_bytes + (((size_t)S * 8 + 15) & ~(size_t)15) + sizeof(int) * kFlagWords;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    umma::mbar_arrive_expect_tx(bar, bytes);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     umma::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <typename StateT, int P, int N>
@@ -181,10 +195,14 @@ __device__ __forceinline__ void store_tile(const float (&st)[Tile<StateT, P, N>:
         __stcs(reinterpret_cast<uint4 *>(base) + pass * TL::TH + th, pack16(st[pass]));
 }
 
+// One CTA per (row, group).  Head tiles of the group are staged into shared memory by bulk
+// asynchronous copies: each head slot (TH threads) owns `sps` stages, so up to sps tiles per slot
+// are in flight while the slot computes; the first copies are issued before the conv phase.
 template <typename StateT, typename ActT, int P, int N, int NT>
 __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     using TL = Tile<StateT, P, N>;
     constexpr int VEC = TL::VEC, VR = TL::VR, TH = TL::TH, RP = TL::RP, PASSES = TL::PASSES;
+    constexpr uint32_t TILE_BYTES = (uint32_t)(P * N * sizeof(StateT));
     const int g = blockIdx.x, i = blockIdx.y;
     const int ntok = NT > 0 ? NT : a.ntok;
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
@@ -204,20 +222,35 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
 
     const int HG = a.HG, LC = HG * P + 2 * N;
     const bool conv = a.conv_pool != nullptr;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *xs = reinterpret_cast<float *>(smem_raw);  // [ntok][LC] x | B | C after the conv
+    const int hs = tid / TH, th = tid - hs * TH, NHS = nthr / TH;
+    const int S = a.sps * NHS;  // stages; head hl uses stage hl % S, which belongs to slot hl % NHS
+    extern __shared__ __align__(128) unsigned char dec_smem[];
+    unsigned char *stages = dec_smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(dec_smem + (size_t)S * TILE_BYTES);
+    const size_t foff = decode_float_offset(S, TILE_BYTES);
+    int *flags = reinterpret_cast<int *>(dec_smem + foff - sizeof(int) * kFlagWords);  // [0, NHS): slot timed out; [NHS]: any
+    float *xs = reinterpret_cast<float *>(dec_smem + foff);  // [ntok][LC] x | B | C after the conv
     float *uraw = xs + ntok * LC;                      // [ntok][LC] raw inputs (conv only)
     float *dl = uraw + (conv ? ntok * LC : 0);         // [ntok][HG] Delta
     float *da = dl + ntok * HG;                        // [ntok][HG] exp(Delta*A)
     float *ys = da + ntok * HG;                        // [ntok][HG*P] C.h
     ActT *cs = reinterpret_cast<ActT *>(ys + ntok * HG * P);  // [LC][Wc] old conv state
 
-    // first head tile's loads go out before the conv phase
-    const int hs = tid / TH, th = tid - hs * TH, NHS = nthr / TH;
-    StateT *grp = static_cast<StateT *>(a.ssm_pool) + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
-    uint4 raw[PASSES];
-    int hl = hs;
-    if (hl < HG) load_tile<StateT, P, N>(raw, grp + (int64_t)hl * P * N, th);
+    if (tid == 0) {
+        for (int st = 0; st < S; ++st) umma::mbar_init(&full[st], 1);
+        umma::fence_mbar_init();
+    }
+    if (tid < kFlagWords) flags[tid] = 0;
+    __syncthreads();
+
+    StateT *pool = static_cast<StateT *>(a.ssm_pool);
+    StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
+    if (th == 0)
+        for (int k = 0; k < a.sps; ++k) {
+            const int hl = hs + k * NHS;
+            if (hl < HG) bulk_load(stages + (size_t)(hl % S) * TILE_BYTES, grp + (int64_t)hl * P * N, TILE_BYTES,
+                                   &full[hl % S]);
+        }
 
     const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * ntok * a.Cd;
     const int HP = a.H * P, GN = a.G * N;
@@ -246,47 +279,105 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     __syncthreads();
 
     const int rsub = th / VR, n0 = (th - rsub * VR) * VEC;
-    for (; hl < HG; hl += NHS) {  // warp-uniform: TH is a multiple of 32
-        float st[PASSES][VEC];
-#pragma unroll
-        for (int pass = 0; pass < PASSES; ++pass) unpack16(raw[pass], st[pass]);
-        for (int j = 0; j < ntok; ++j) {
-            const float dA = da[j * HG + hl], dlt = dl[j * HG + hl];
-            const float *xj = xs + j * LC;
+    int hl = hs;
+    for (; hl < HG; hl += NHS) {  // slot-uniform: TH is a multiple of 32
+        const int stg = hl % S;
+        if (th == 0 && !umma::mbar_wait(&full[stg], (uint32_t)(hl / S) & 1u, kMaxPolls)) flags[hs] = 1;
+        named_sync(1 + hs, TH);
+        if (flags[hs]) break;
+        const uint4 *tile = reinterpret_cast<const uint4 *>(stages + (size_t)stg * TILE_BYTES);
+        float part[PASSES];
+        if constexpr (NT == 1) {
+            // single token: stream the tile through registers vector by vector
+            const float dA = da[hl], dlt = dl[hl];
             float Bv[VEC], Cv[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; e += 4) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(xj + HG * P + n0 + e);
-                const float4 c4 = *reinterpret_cast<const float4 *>(xj + HG * P + N + n0 + e);
+                const float4 b4 = *reinterpret_cast<const float4 *>(xs + HG * P + n0 + e);
+                const float4 c4 = *reinterpret_cast<const float4 *>(xs + HG * P + N + n0 + e);
                 Bv[e] = b4.x; Bv[e + 1] = b4.y; Bv[e + 2] = b4.z; Bv[e + 3] = b4.w;
                 Cv[e] = c4.x; Cv[e + 1] = c4.y; Cv[e + 2] = c4.z; Cv[e + 3] = c4.w;
             }
-            float part[PASSES];
+            StateT *dst = grp + (int64_t)hl * P * N;
+            if (a.scratch) {
+                const int32_t d = a.scratch[i];
+                dst = d >= 0 ? pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N : nullptr;
+            }
 #pragma unroll
             for (int pass = 0; pass < PASSES; ++pass) {
-                const float dtx = dlt * xj[hl * P + pass * RP + rsub];
+                float f[VEC];
+                unpack16(tile[pass * TH + th], f);
+                const float dtx = dlt * xs[hl * P + pass * RP + rsub];
                 float acc = 0.0f;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    st[pass][e] = fmaf(dA, st[pass][e], dtx * Bv[e]);
-                    acc = fmaf(Cv[e], st[pass][e], acc);
+                    f[e] = fmaf(dA, f[e], dtx * Bv[e]);
+                    acc = fmaf(Cv[e], f[e], acc);
                 }
                 part[pass] = acc;
+                if (dst) __stcs(reinterpret_cast<uint4 *>(dst) + pass * TH + th, pack16(f));
             }
+            named_sync(1 + hs, TH);  // every thread of the slot has read the stage
+            if (th == 0 && hl + S < HG)
+                bulk_load(stages + (size_t)stg * TILE_BYTES, grp + (int64_t)(hl + S) * P * N, TILE_BYTES, &full[stg]);
             int idx = 0;
             ReduceScatter<PASSES, VR / 2>::run(part, lane, idx);
-            if ((lane & (VR / PASSES - 1)) == 0) ys[j * HG * P + hl * P + idx * RP + rsub] = part[0];
-            if (a.scratch) {
-                const int32_t d = a.scratch[(int64_t)i * ntok + j];
-                if (d >= 0)
-                    store_tile<StateT, P, N>(st, static_cast<StateT *>(a.ssm_pool) + (int64_t)d * a.ssm_stride +
-                                                     (int64_t)(g * HG + hl) * P * N, th);
+            if ((lane & (VR / PASSES - 1)) == 0) ys[hl * P + idx * RP + rsub] = part[0];
+        } else {
+            // several tokens: the tile stays in fp32 registers across them
+            float st[PASSES][VEC];
+#pragma unroll
+            for (int pass = 0; pass < PASSES; ++pass) unpack16(tile[pass * TH + th], st[pass]);
+            named_sync(1 + hs, TH);
+            if (th == 0 && hl + S < HG)
+                bulk_load(stages + (size_t)stg * TILE_BYTES, grp + (int64_t)(hl + S) * P * N, TILE_BYTES, &full[stg]);
+            for (int j = 0; j < ntok; ++j) {
+                const float dA = da[j * HG + hl], dlt = dl[j * HG + hl];
+                const float *xj = xs + j * LC;
+                float Bv[VEC], Cv[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; e += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(xj + HG * P + n0 + e);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(xj + HG * P + N + n0 + e);
+                    Bv[e] = b4.x; Bv[e + 1] = b4.y; Bv[e + 2] = b4.z; Bv[e + 3] = b4.w;
+                    Cv[e] = c4.x; Cv[e + 1] = c4.y; Cv[e + 2] = c4.z; Cv[e + 3] = c4.w;
+                }
+#pragma unroll
+                for (int pass = 0; pass < PASSES; ++pass) {
+                    const float dtx = dlt * xj[hl * P + pass * RP + rsub];
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        st[pass][e] = fmaf(dA, st[pass][e], dtx * Bv[e]);
+                        acc = fmaf(Cv[e], st[pass][e], acc);
+                    }
+                    part[pass] = acc;
+                }
+                int idx = 0;
+                ReduceScatter<PASSES, VR / 2>::run(part, lane, idx);
+                if ((lane & (VR / PASSES - 1)) == 0) ys[j * HG * P + hl * P + idx * RP + rsub] = part[0];
+                if (a.scratch) {
+                    const int32_t d = a.scratch[(int64_t)i * ntok + j];
+                    if (d >= 0)
+                        store_tile<StateT, P, N>(st, pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N,
+                                                 th);
+                }
             }
+            if (!a.scratch) store_tile<StateT, P, N>(st, grp + (int64_t)hl * P * N, th);
         }
-        if (!a.scratch) store_tile<StateT, P, N>(st, grp + (int64_t)hl * P * N, th);
-        if (hl + NHS < HG) load_tile<StateT, P, N>(raw, grp + (int64_t)(hl + NHS) * P * N, th);
+    }
+    if (hl < HG) {
+        // a copy did not land in time: report it, let this slot's copies that are still in flight
+        // finish (bounded), and skip the outputs of this row
+        if (th == 0) {
+            flag_error(a.err, MAMBA_ERR_TIMEOUT);
+            flags[NHS] = 1;
+            for (int h2 = hl + NHS; h2 < HG && h2 < hl + S; h2 += NHS)
+                umma::mbar_wait(&full[h2 % S], (uint32_t)(h2 / S) & 1u, kMaxPolls);
+        }
     }
     __syncthreads();
+    if (flags[NHS]) return;
 
     // y = C.h + D*x, gated by SiLU(z)
     const ActT *zr = static_cast<const ActT *>(a.z);
@@ -412,16 +503,25 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 // ---------------------------------------------------------------------------------------
 
 template <typename StateT, typename ActT, int P, int N>
-static int launch_decode_shape(const DecodeArgs &a, int ntok, int P_, int N_, cudaStream_t stream) {
+static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, cudaStream_t stream) {
     using TL = Tile<StateT, P, N>;
+    DecodeArgs a = a0;
     const int LC = a.HG * P + 2 * N;
     const bool conv = a.conv_pool != nullptr;
-    const size_t smem = sizeof(float) * (size_t)decode_smem_floats(ntok, LC, a.HG, P, conv) +
-                        (conv ? sizeof(ActT) * (size_t)LC * a.Wc : 0);
-    if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
     int nhs = 256 / TL::TH;
     if (nhs < 1) nhs = 1;
     if (nhs > a.HG) nhs = a.HG;
+    if (nhs > 8) nhs = 8;
+    const size_t tile = (size_t)P * N * sizeof(StateT);
+    const size_t rest = sizeof(float) * (size_t)decode_smem_floats(ntok, LC, a.HG, P, conv) +
+                        (conv ? sizeof(ActT) * (size_t)LC * a.Wc : 0);
+    // two stages per head slot (up to 2 * nhs tiles in flight per CTA), fewer if shared memory is short
+    int sps = 2;
+    auto smem_for = [&](int k) { return decode_float_offset(k * nhs, tile) + rest; };
+    while (sps > 1 && smem_for(sps) > 227 * 1024) --sps;
+    const size_t smem = smem_for(sps);
+    if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
+    a.sps = sps;
     const dim3 grid(a.G, a.batch), block(nhs * TL::TH);
     auto kern = ntok == 1 ? k_decode<StateT, ActT, P, N, 1> : k_decode<StateT, ActT, P, N, 0>;
     if (smem > 48 * 1024) {

@@ -100,8 +100,11 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     d = bd.layer_desc(wl.NEMOTRON_H_8B)
-    ws = bd.mamba_chunk_scan_workspace_bytes(d, 32768, 8, 256)
-    # at least the per-chunk fp32 states of every chunk (each sequence adds <= 1 partial chunk)
+    # tensor-core layer (bf16, head_dim 64, d_state 128): only the sequence order is kept
+    assert 0 < bd.mamba_chunk_scan_workspace_bytes(d, 32768, 8, 256) <= 4096
+    # portable layer (fp32 activations): at least the per-chunk fp32 states of every chunk
+    d32 = bd.layer_desc(wl.NEMOTRON_H_8B, state=wl.F32, act=wl.F32)
+    ws = bd.mamba_chunk_scan_workspace_bytes(d32, 32768, 8, 256)
     assert ws >= (32768 // 256 + 8) * 128 * 64 * 128 * 4
     assert bd.mamba_chunk_scan_workspace_bytes(d, -1, 8, 256) == 0
 
@@ -178,6 +181,6 @@ def test_chunk_scan_host_errors(lib):
     assert call(ssm=None) == bd.MAMBA_EINVAL
     assert call(ws=None) == bd.MAMBA_EINVAL
     assert call(wsb=need - 1) == bd.MAMBA_ENOSPACE
-    assert call(chunk=128) == bd.MAMBA_EUNSUPPORTED
+    assert call(chunk=100) == bd.MAMBA_EUNSUPPORTED  # neither a tensor-core nor a portable chunk
     assert call(ck=FAKE, mc=4, ci=1000) == bd.MAMBA_EINVAL  # interval not a multiple of the chunk
     assert call(ws=FAKE + 4) == bd.MAMBA_EALIGN

@@ -132,6 +132,33 @@ def test_prefill_fp32_varlen_edges():
     pr.check(1e-4)
 
 
+def test_prefill_tc_edges():
+    """Tensor-core path: empty, length-1, 128/256-multiple and partial sequences, initial states,
+    checkpoints, z gate."""
+    pr = Problem(wl.NEMOTRON_H_8B, [1, 0, 128, 129, 256, 300, 1024], seed=5, act=wl.BF16, state=wl.BF16,
+                 has_init=[1, 1, 0, 1, 0, 1, 1], interval=256, with_z=True)
+    pr.run_gpu()
+    pr.check(2e-2)
+
+
+def test_prefill_tc_fp32_state():
+    """Tensor-core path with an fp32 state pool (bf16 activations)."""
+    pr = Problem(wl.NEMOTRON_H_8B, [513, 1000], seed=6, act=wl.BF16, state=wl.F32, has_init=[1, 0], interval=512)
+    pr.run_gpu()
+    pr.check(2e-2)
+
+
+def test_prefill_tc_bad_seqlens_flagged_nothing_written():
+    import torch
+    pr = Problem(wl.NEMOTRON_H_8B, [100, 50], seed=9, act=wl.BF16, state=wl.BF16)
+    pr.cu = np.array([0, 160, 150], np.int32)  # decreasing
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pr.run_gpu(err)
+    assert int(err.item()) & bd.MAMBA_ERR_SEQLENS
+    np.testing.assert_array_equal(f64(pr.pool), wl.upcast(pr.pool0, wl.BF16))
+    assert not f64(pr.y).any()
+
+
 def test_prefill_bf16_nemotron_shape():
     pr = Problem(wl.NEMOTRON_H_8B, [700, 1064, 33], seed=2, act=wl.BF16, state=wl.BF16, has_init=[1, 0, 1],
                  interval=512)

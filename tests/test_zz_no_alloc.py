@@ -86,13 +86,14 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
 
 def test_noalloc_refuses_a_problem_larger_than_its_scratch():
     import torch
-    desc = bd.layer_desc(wl.NEMOTRON_H_8B)
+    # fp32 activations take the portable path, whose scratch grows with the number of chunks
+    desc = bd.layer_desc(wl.NEMOTRON_H_8B, state=wl.F32, act=wl.F32)
     limit = bd.mamba_chunk_scan_static_scratch_bytes()
-    T = 64 * 1024  # needs far more workspace than the fixed scratch holds
+    T = 8192  # 32 chunks of per-chunk fp32 states: more than the fixed scratch holds
     assert bd.mamba_chunk_scan_workspace_bytes(desc, T, 1, 256) > limit
     one = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pool = torch.zeros(1, 128, 64, 128, dtype=torch.bfloat16, device="cuda")
-    x = torch.zeros(T, 128, 64, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(1, 128, 64, 128, dtype=torch.float32, device="cuda")
+    x = torch.zeros(T, 128, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(bd.MambaError) as e:
         bd.mamba_chunk_scan_noalloc(desc, pool, to_i32(np.array([0, T])), one, x, one, one, one, one, x)
     assert e.value.status == bd.MAMBA_ENOSPACE
