@@ -86,7 +86,10 @@ def _profile_traffic(kernel: str):
     for line in text.splitlines():
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`") and v.count("`") >= 2:
+                v = v[1:v.index("`", 1)]  # the value is the first backticked field
+            vals[k.strip()] = v
     src = vals.get("source")
     if not src or "traffic_bytes_per_launch" not in vals:
         return None
@@ -113,7 +116,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -281,12 +284,18 @@ def _time(torch, fn, steps, warmup, dist=None):
     return e0.elapsed_time(e1) / steps  # ms per step
 
 
-def _max_over_ranks(torch, dist, v):
+def _max_over_ranks(torch, dist, v, device="cuda"):
+    """The slowest rank's time: every rank contributes its own, all get the maximum."""
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job GB/s: the bytes all ranks moved over the slowest rank's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
 
 
 def cpu_baseline_decode(budget_s: float = 10.0, rows: int = 32):
@@ -344,16 +353,17 @@ def run_gpu(args):
     layers = args.layers or DECODE["layers"]
     dec = DecodeWorkload(torch, rank, layers, DECODE["batch"], DECODE["pool"])
     clocks = ClockSampler(local)
+    # the sampler runs across the warm-up and the timed steps, so its samples see the GPU under load
+    clocks.start()
+    time.sleep(0.2)
     for _ in range(args.warmup):
         dec.step()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     ms = _time(torch, dec.step, args.steps, 0, dist)
     ck = clocks.stop()
     ms = _max_over_ranks(torch, dist, ms)
     total_bytes = dec.bytes_per_step() * world
-    value = total_bytes / (ms * 1e-3) / 1e9
+    value = weak_scaling_gbs(dec.bytes_per_step(), world, ms)
     token_layers = layers * DECODE["batch"] * world / (ms * 1e-3)
     launch_ms = ms / dec.launches_per_step
     achieved = DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER / (launch_ms * 1e-3) / 1e9
@@ -401,30 +411,29 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
 
 
 def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
-         cpu):
-    if True:
-        line = {
-            "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
-            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
-            "config": {"workload": DECODE["name"], "layers": layers, "global_batch": DECODE["batch"] * world,
-                       "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
-                       "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
-                       "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"},
-            "token_layers_per_s": token_layers,
-            "roofline": {"bound": "hbm", "kernel": "k_decode", "achieved": achieved, "peak": hbm_peak,
-                         "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_src,
-                         "traffic": _profile_traffic("decode_nemotron_b256"),
-                         "algorithmic_bytes_per_launch": DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER,
-                         "avg_launch_ms": launch_ms},
-            "e2e": e2e,
-            "gpu_launches": args.steps * layers,
-            "clocks": ck,
-            "prefill": prefill,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
+     cpu):
+    line = {
+        "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": DECODE["name"], "layers": layers, "global_batch": DECODE["batch"] * world,
+                   "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
+                   "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
+                   "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"},
+        "token_layers_per_s": token_layers,
+        "roofline": {"bound": "hbm", "kernel": "k_decode_stream", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "traffic": _profile_traffic("decode_nemotron_b256"),
+                     "algorithmic_bytes_per_launch": DECODE["batch"] * DECODE_BYTES_PER_TOKEN_LAYER,
+                     "avg_launch_ms": launch_ms},
+        "e2e": e2e,
+        "gpu_launches": args.steps * layers,
+        "clocks": ck,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------------------------
@@ -481,7 +490,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")

@@ -198,13 +198,29 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
     bool h_valid = has_init;
     bool failed = false;
     uint32_t ph = 0;
+    // dt of the sub-chunk about to run (prefetched one sub-chunk ahead)
+    float dt_next = tid < min(SQ, len) ? load_scalar(p.dt, (int64_t)(t_begin + tid) * p.H + h, p.dt_bf16) : 0.0f;
     for (int k = 0; k < nsub; ++k, ph ^= 1u) {
         const int t0 = t_begin + k * SQ, L = min(SQ, len - k * SQ);
+        // the gate row of this thread's token, fetched now and used by the epilogue
+        uint4 zrow[8];
+        if (p.z && tid < L) {
+            const uint4 *zr = reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(p.z) +
+                                                              ((int64_t)(t0 + tid) * p.H + h) * TP);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) zrow[q] = zr[q];
+        }
         // Delta and the within-sub-chunk cumulative sum of Delta*A (thread = token)
         float dlt = 0.0f;
         if (tid < L) {
-            const float sdt = load_scalar(p.dt, (int64_t)(t0 + tid) * p.H + h, p.dt_bf16) + bias;
+            const float sdt = dt_next + bias;
             dlt = p.dt_softplus ? softplus_f(sdt) : sdt;
+        }
+        {
+            const int Ln = min(SQ, len - (k + 1) * SQ);
+            dt_next = (k + 1 < nsub && tid < Ln)
+                          ? load_scalar(p.dt, (int64_t)(t0 + SQ + tid) * p.H + h, p.dt_bf16)
+                          : 0.0f;
         }
         float run = dlt * Ah;
 #pragma unroll
@@ -245,6 +261,10 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
         }
         const float cend = sv->cum2[L - 1];
         sv->w[tid] = tid < L ? exp2f(cend - sv->cum2[tid]) * dlt : 0.0f;
+        // this thread's token row of X (for D x), read before the tile is scaled in place
+        uint4 xrow[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xrow[q] = *reinterpret_cast<const uint4 *>(sm + OFF_X + swz128_chunk(tid, q));
 
         // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, into the C buffer (C is consumed)
         bad = !mbar_wait(&sv->bar_g, ph, kPolls);
@@ -350,9 +370,9 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
             const int i = tid;
             const float ei = exp2f(sv->cum2[i]);
             const int64_t row = ((int64_t)(t0 + i) * p.H + h) * TP;
-            const bf16 *xr = static_cast<const bf16 *>(p.x) + row;
-            const bf16 *zr = p.z ? static_cast<const bf16 *>(p.z) + row : nullptr;
+            const bool gate = p.z != nullptr;
             bf16 *yr = static_cast<bf16 *>(p.y) + row;
+#pragma unroll
             for (int c0 = 0; c0 < TP; c0 += 32) {
                 float yd[32], yo[32];
                 tmem_ld32(t_yd + lane_base + c0, yd);
@@ -365,9 +385,8 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
                 if (i < L) {
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xr + c0 + 8 * q8);
-                        uint4 zv = make_uint4(0, 0, 0, 0);
-                        if (zr) zv = *reinterpret_cast<const uint4 *>(zr + c0 + 8 * q8);
+                        const uint4 xv = xrow[c0 / 8 + q8];
+                        const uint4 zv = gate ? zrow[c0 / 8 + q8] : make_uint4(0, 0, 0, 0);
                         const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv);
                         const uint32_t *zw = reinterpret_cast<const uint32_t *>(&zv);
                         uint4 out;
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
                             const int q = 8 * q8 + 2 * e;
                             float v0 = yd[q] + ei * yo[q] + Dh * __uint_as_float(xw[e] << 16);
                             float v1 = yd[q + 1] + ei * yo[q + 1] + Dh * __uint_as_float(xw[e] & 0xffff0000u);
-                            if (zr) {
+                            if (gate) {
                                 v0 *= silu_f(__uint_as_float(zw[e] << 16));
                                 v1 *= silu_f(__uint_as_float(zw[e] & 0xffff0000u));
                             }

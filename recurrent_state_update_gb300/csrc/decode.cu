@@ -394,6 +394,326 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------
+// single-token decode as a persistent, warp-specialised stream
+// ---------------------------------------------------------------------------------------
+//
+// Work item = (row, group).  Each CTA walks the items b, b + gridDim, ... with three roles:
+//   producer warp:   bulk-copies the state tiles of its items, in order, into a ring of NS
+//                    shared-memory stages, running ahead of the consumers by up to NS tiles
+//                    (across item boundaries, so the copies never stop at an item's edge);
+//   conv warps:      for the next item, the causal conv + SiLU of the group's x|B|C channels,
+//                    the conv-state shift, Delta / exp(Delta*A) and the z gate values, into one
+//                    of two per-item buffers;
+//   consumer warps:  per tile, h <- exp(Delta*A) h + Delta x B^T, C.h, the state write-back, and
+//                    after all of an item's heads, y = C.h + D x gated by SiLU(z).
+// All waits are bounded: a wait that gives up sets the CTA's abort flag, every role stops, and
+// the copies still in flight are drained (bounded) before the CTA exits.
+
+constexpr int kStreamConsumers = 256;  // consumer threads (head slots of TH threads)
+constexpr int kStreamConv = 64;        // conv threads
+constexpr int kStreamThreads = kStreamConsumers + kStreamConv + 32;
+
+struct StreamArgs {
+    DecodeArgs d;
+    int ns;  // tile stages
+};
+
+// per-item buffer: xs[LC] | dl[HG] | da[HG] | zf[HG*P] | ys[HG*P]   (floats), rounded up to 16 bytes so
+// that both buffers keep the float4 alignment of xs
+__host__ __device__ inline int stream_item_floats(int LC, int HG, int P) {
+    return (LC + 2 * HG + 2 * HG * P + 3) & ~3;
+}
+
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// Shared-memory map of the stream kernel (byte offsets).
+struct StreamSmem {
+    size_t bars, flags, items, wsm, cs, ur, zr, total;
+    __host__ __device__ StreamSmem(int ns, size_t tile, int LC, int HG, int P, int W, int Wc, size_t es) {
+        bars = (size_t)ns * tile;                       // stages first (16-byte aligned tiles)
+        flags = align16(bars + 8 * (size_t)(2 * ns + 7));  // full/empty, xs_full/empty, cons, conv, conv_in
+        items = flags + 16;                             // abort, issued, cached tap group
+        wsm = items + sizeof(float) * 2 * (size_t)stream_item_floats(LC, HG, P);
+        cs = align16(wsm + sizeof(float) * (size_t)LC * W);  // conv taps of the cached group
+        ur = align16(cs + es * (size_t)LC * Wc);        // old conv state of the item
+        zr = align16(ur + es * (size_t)LC);             // raw inputs of the item
+        total = align16(zr + es * (size_t)HG * P);      // z row of the item
+    }
+};
+
+__device__ __forceinline__ bool stream_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        if (umma::mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 1023u && *abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(bar)) : "memory");
+}
+
+// Bounded barrier among the members of one role: each member arrives, then waits for the phase.
+// (No hardware named barrier is used inside the stream kernel, so a member that gives up can never
+// leave the others blocked.)
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, volatile int *abort) {
+    mbar_arrive(bar);
+    const bool ok = stream_wait(bar, phase & 1u, abort);
+    ++phase;
+    return ok;
+}
+
+// Bulk copy without expect_tx (the caller posts the total once).
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     umma::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
+                 : "memory");
+}
+
+template <typename StateT, typename ActT, int P, int N>
+__global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const StreamArgs sa) {
+    using TL = Tile<StateT, P, N>;
+    constexpr int VEC = TL::VEC, VR = TL::VR, TH = TL::TH, RP = TL::RP, PASSES = TL::PASSES;
+    constexpr int NHS = kStreamConsumers / TH;
+    constexpr uint32_t TILE_BYTES = (uint32_t)(P * N * sizeof(StateT));
+    constexpr int ES = (int)sizeof(ActT);
+    const DecodeArgs &a = sa.d;
+    const int NS = sa.ns, HG = a.HG, LC = HG * P + 2 * N, G = a.G, Wk = a.W, Wc = a.Wc;
+    const int HP = a.H * P, GN = a.G * N;
+    const int tid = threadIdx.x;
+    const int W = a.batch * G;
+    const StreamSmem L(NS, TILE_BYTES, LC, HG, P, Wk, Wc, ES);
+
+    extern __shared__ __align__(128) unsigned char st_smem[];
+    unsigned char *stages = st_smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(st_smem + L.bars);
+    uint64_t *empty = full + NS;
+    uint64_t *xs_full = empty + NS;    // [2]
+    uint64_t *xs_empty = xs_full + 2;  // [2]
+    uint64_t *cons_bar = xs_empty + 2;
+    uint64_t *conv_bar = cons_bar + 1;
+    uint64_t *conv_in = conv_bar + 1;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(st_smem + L.flags);
+    int *issued = reinterpret_cast<int *>(st_smem + L.flags) + 1;  // tiles issued by the producer
+    float *items = reinterpret_cast<float *>(st_smem + L.items);
+    const int IF = stream_item_floats(LC, HG, P);
+    float *wsm = reinterpret_cast<float *>(st_smem + L.wsm);
+    ActT *cs = reinterpret_cast<ActT *>(st_smem + L.cs);
+    ActT *ur = reinterpret_cast<ActT *>(st_smem + L.ur);
+    ActT *zr = reinterpret_cast<ActT *>(st_smem + L.zr);
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            umma::mbar_init(&full[s], 1);
+            umma::mbar_init(&empty[s], TH);
+        }
+        for (int e = 0; e < 2; ++e) {
+            umma::mbar_init(&xs_full[e], kStreamConv);
+            umma::mbar_init(&xs_empty[e], kStreamConsumers);
+        }
+        umma::mbar_init(cons_bar, kStreamConsumers);
+        umma::mbar_init(conv_bar, kStreamConv);
+        umma::mbar_init(conv_in, 1);
+        umma::fence_mbar_init();
+        *abort_flag = 0;
+        *issued = 0;
+    }
+    __syncthreads();
+
+    StateT *pool = static_cast<StateT *>(a.ssm_pool);
+    // the slot of an item, or -1 when the item is skipped (padding row, or a slot outside the pool)
+    auto item_slot = [&](int w) -> int32_t {
+        const int32_t s = a.slot[w / G];
+        return (s >= 0 && s < a.num_slots) ? s : -1;
+    };
+
+    if (tid >= kStreamConsumers + kStreamConv) {
+        // ---------------- producer warp ----------------
+        if (tid == kStreamConsumers + kStreamConv) {
+            int t = 0;
+            for (int w = blockIdx.x; w < W && !*abort_flag; w += gridDim.x) {
+                const int32_t s = a.slot[w / G];
+                if (s >= a.num_slots && w % G == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+                if (s < 0 || s >= a.num_slots) continue;
+                const StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)(w % G) * HG * P * N;
+                for (int hl = 0; hl < HG; ++hl, ++t) {
+                    const int st = t % NS;
+                    if (t >= NS && !stream_wait(&empty[st], (uint32_t)(t / NS - 1) & 1u, abort_flag)) break;
+                    bulk_load(stages + (size_t)st * TILE_BYTES, grp + (int64_t)hl * P * N, TILE_BYTES, &full[st]);
+                }
+                *issued = t;
+            }
+            *issued = t;
+        }
+    } else if (tid >= kStreamConsumers) {
+        // ---------------- conv warps ----------------
+        // the item's inputs arrive by bulk copies (conv state and xBC of the group's channels in
+        // the order x | B | C, the z row, and the group's conv taps when the group changes)
+        const int ct = tid - kStreamConsumers;
+        uint32_t cph = 0, iph = 0;
+        int n = 0, wgroup = -1;
+        const size_t xseg = (size_t)HG * P, bseg = N;  // channels per segment
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const int32_t s = item_slot(w);
+            if (s < 0) continue;
+            const int e = n & 1;
+            if (n >= 2 && !stream_wait(&xs_empty[e], (uint32_t)(n / 2 - 1) & 1u, abort_flag)) break;
+            if (*abort_flag) break;
+            const int i = w / G, g = w % G;
+            const int lo[3] = {g * HG * P, HP + g * N, HP + GN + g * N};
+            const size_t len[3] = {xseg, bseg, bseg};
+            if (ct == 0) {
+                uint32_t bytes = (uint32_t)((size_t)LC * Wc * ES + (size_t)LC * ES + (a.z ? (size_t)HG * P * ES : 0));
+                if (wgroup != g) bytes += (uint32_t)(sizeof(float) * (size_t)LC * Wk);
+                umma::fence_async_smem();
+                umma::mbar_arrive_expect_tx(conv_in, bytes);
+                const ActT *cstate = static_cast<const ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+                const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * a.Cd;
+                size_t base = 0;
+                for (int r = 0; r < 3; ++r) {
+                    bulk_copy(cs + base * Wc, cstate + (int64_t)lo[r] * Wc, (uint32_t)(len[r] * Wc * ES), conv_in);
+                    bulk_copy(ur + base, u_row + lo[r], (uint32_t)(len[r] * ES), conv_in);
+                    if (wgroup != g)
+                        bulk_copy(wsm + base * Wk, a.conv_w + (int64_t)lo[r] * Wk, (uint32_t)(len[r] * Wk * sizeof(float)),
+                                  conv_in);
+                    base += len[r];
+                }
+                if (a.z)
+                    bulk_copy(zr, static_cast<const ActT *>(a.z) + (int64_t)i * HP + (int64_t)g * HG * P,
+                              (uint32_t)((size_t)HG * P * ES), conv_in);
+            }
+            wgroup = g;
+            if (!stream_wait(conv_in, iph & 1u, abort_flag)) break;
+            ++iph;
+            float *xs = items + e * IF, *dl = xs + LC, *da = dl + HG, *zf = da + HG;
+            for (int lc = ct; lc < LC; lc += kStreamConv) {
+                const int r = lc < (int)xseg ? 0 : (lc < (int)(xseg + bseg) ? 1 : 2);
+                const int c = lo[r] + lc - (r == 0 ? 0 : (r == 1 ? (int)xseg : (int)(xseg + bseg)));
+                float v = a.conv_b ? a.conv_b[c] : 0.0f;
+                for (int k = 0; k < Wk; ++k) {
+                    const int m = Wc - (Wk - 1) + k;
+                    const float val = m < Wc ? to_f32(cs[lc * Wc + m]) : to_f32(ur[lc]);
+                    v = fmaf(wsm[lc * Wk + k], val, v);
+                }
+                xs[lc] = silu_f(v);
+            }
+            for (int hl = ct; hl < HG; hl += kStreamConv) {
+                const int h = g * HG + hl;
+                const float sdt = load_scalar(a.dt, (int64_t)i * a.H + h, a.dt_bf16) + (a.dt_bias ? a.dt_bias[h] : 0.0f);
+                const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
+                dl[hl] = delta;
+                da[hl] = expf(delta * a.A[h]);
+            }
+            if (a.z)
+                for (int q = ct; q < HG * P; q += kStreamConv) zf[q] = to_f32(zr[q]);
+            // the shifted conv state, 16 bytes per store: new column k is old column k+1, the last is the input
+            {
+                ActT *cstate = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+                constexpr int VE = 16 / ES;
+                size_t base = 0;
+                for (int r = 0; r < 3; ++r) {
+                    const int nv = (int)(len[r] * Wc / VE);
+                    uint4 *dst = reinterpret_cast<uint4 *>(cstate + (int64_t)lo[r] * Wc);
+                    for (int v = ct; v < nv; v += kStreamConv) {
+                        ActT out[VE];
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) {
+                            const int el = v * VE + q, lcl = el / Wc, k = el - lcl * Wc;
+                            out[q] = k + 1 < Wc ? cs[(base + lcl) * Wc + k + 1] : ur[base + lcl];
+                        }
+                        dst[v] = *reinterpret_cast<const uint4 *>(out);
+                    }
+                    base += len[r];
+                }
+            }
+            mbar_arrive(&xs_full[e]);
+            if (!group_sync(conv_bar, cph, abort_flag)) break;  // cs / ur / zr / taps are refilled next
+            ++n;
+        }
+    } else {
+        // ---------------- consumer warps ----------------
+        const int hs = tid / TH, th = tid - hs * TH, lane = tid & 31;
+        const int rsub = th / VR, n0 = (th - rsub * VR) * VEC;
+        uint32_t bph = 0;
+        int n = 0, t0 = 0;
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const int32_t s = item_slot(w);
+            if (s < 0) continue;
+            const int e = n & 1;
+            if (!stream_wait(&xs_full[e], (uint32_t)(n / 2) & 1u, abort_flag)) break;
+            const int i = w / G, g = w % G;
+            float *xs = items + e * IF, *dl = xs + LC, *da = dl + HG, *zf = da + HG, *ys = zf + HG * P;
+            StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
+            float Bv[VEC], Cv[VEC];
+#pragma unroll
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(xs + HG * P + n0 + q);
+                const float4 c4 = *reinterpret_cast<const float4 *>(xs + HG * P + N + n0 + q);
+                Bv[q] = b4.x; Bv[q + 1] = b4.y; Bv[q + 2] = b4.z; Bv[q + 3] = b4.w;
+                Cv[q] = c4.x; Cv[q + 1] = c4.y; Cv[q + 2] = c4.z; Cv[q + 3] = c4.w;
+            }
+            bool stop = false;
+            for (int hl = hs; hl < HG; hl += NHS) {
+                const int t = t0 + hl, st = t % NS;
+                if (!stream_wait(&full[st], (uint32_t)(t / NS) & 1u, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                const uint4 *tile = reinterpret_cast<const uint4 *>(stages + (size_t)st * TILE_BYTES);
+                uint4 raw[PASSES];
+#pragma unroll
+                for (int pass = 0; pass < PASSES; ++pass) raw[pass] = tile[pass * TH + th];
+                mbar_arrive(&empty[st]);  // the stage can be refilled
+                const float dA = da[hl], dlt = dl[hl];
+                StateT *dst = grp + (int64_t)hl * P * N;
+                float part[PASSES];
+#pragma unroll
+                for (int pass = 0; pass < PASSES; ++pass) {
+                    float f[VEC];
+                    unpack16(raw[pass], f);
+                    const float dtx = dlt * xs[hl * P + pass * RP + rsub];
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) {
+                        f[q] = fmaf(dA, f[q], dtx * Bv[q]);
+                        acc = fmaf(Cv[q], f[q], acc);
+                    }
+                    part[pass] = acc;
+                    __stcs(reinterpret_cast<uint4 *>(dst) + pass * TH + th, pack16(f));
+                }
+                int idx = 0;
+                ReduceScatter<PASSES, VR / 2>::run(part, lane, idx);
+                if ((lane & (VR / PASSES - 1)) == 0) ys[hl * P + idx * RP + rsub] = part[0];
+            }
+            if (stop) break;
+            if (!group_sync(cons_bar, bph, abort_flag)) break;  // every head of the item is reduced
+            ActT *yr = static_cast<ActT *>(a.y) + (int64_t)i * HP + (int64_t)g * HG * P;
+            for (int q = tid; q < HG * P; q += kStreamConsumers) {
+                const int h = g * HG + q / P;
+                const float xv = xs[q];
+                float yv = ys[q] + (a.D ? a.D[h] * xv : 0.0f);
+                if (a.z) yv *= silu_f(zf[q]);
+                yr[q] = from_f32<ActT>(yv);
+            }
+            mbar_arrive(&xs_empty[e]);
+            t0 += HG;
+            ++n;
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag) {
+        // report, and let every copy this CTA issued land before its shared memory is released
+        flag_error(a.err, MAMBA_ERR_TIMEOUT);
+        const int ti = *issued;
+        for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t) umma::mbar_wait(&full[t % NS], (uint32_t)(t / NS) & 1u, kMaxPolls);
+        umma::mbar_wait(conv_in, 0u, 1024);
+        umma::mbar_wait(conv_in, 1u, 1024);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // standalone conv update
 // ---------------------------------------------------------------------------------------
 
@@ -502,6 +822,45 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 // host side
 // ---------------------------------------------------------------------------------------
 
+// Persistent single-token launch: as many stages as fit beside the item buffers, one CTA per SM.
+// Returns 1 when the layer's conv / xBC / z segments are not 16-byte aligned for bulk copies (the
+// caller then uses the per-item kernel).
+template <typename StateT, typename ActT, int P, int N>
+static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
+    const int LC = a.HG * P + 2 * N;
+    const size_t es = sizeof(ActT), tile = (size_t)P * N * sizeof(StateT);
+    const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N, HGP = (size_t)a.HG * P;
+    auto a16 = [](size_t v) { return v % 16 == 0; };
+    auto p16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const bool aligned = a.conv_pool && p16(a.conv_pool) && p16(a.xbc) && p16(a.conv_w) && (!a.z || p16(a.z)) &&
+                         a16((size_t)a.conv_stride * es) && a16(HGP * a.Wc * es) && a16((size_t)N * a.Wc * es) &&
+                         a16(HP * a.Wc * es) && a16(GN * a.Wc * es) && a16((size_t)a.Cd * es) && a16(HGP * es) &&
+                         a16((size_t)N * es) && a16(HP * es) && a16(GN * es) && a16(HGP * a.W * 4) &&
+                         a16((size_t)N * a.W * 4) && a16(HP * a.W * 4) && a16(GN * a.W * 4);
+    if (!aligned) return 1;
+    int ns = 16;
+    while (ns > 2 && StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es).total > 220 * 1024) --ns;
+    const size_t smem = StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es).total;
+    if (smem > 227 * 1024) return 1;
+    static int sm_count = 0;
+    if (sm_count == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MAMBA_ECUDA;
+    }
+    StreamArgs sa;
+    sa.d = a;
+    sa.ns = ns;
+    const int W = a.batch * a.G;
+    const int grid = W < sm_count ? W : sm_count;
+    auto kern = k_decode_stream<StateT, ActT, P, N>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MAMBA_ECUDA;
+    kern<<<grid, kStreamThreads, smem, stream>>>(sa);
+    return launch_status();
+}
+
 template <typename StateT, typename ActT, int P, int N>
 static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, cudaStream_t stream) {
     using TL = Tile<StateT, P, N>;
@@ -522,6 +881,12 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     const size_t smem = smem_for(sps);
     if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
     a.sps = sps;
+    if constexpr (TL::TH <= kStreamConsumers && kStreamConsumers % TL::TH == 0) {
+        if (ntok == 1 && a.scratch == nullptr) {
+            const int rc = launch_stream<StateT, ActT, P, N>(a, stream);
+            if (rc != 1) return rc;
+        }
+    }
     const dim3 grid(a.G, a.batch), block(nhs * TL::TH);
     auto kern = ntok == 1 ? k_decode<StateT, ActT, P, N, 1> : k_decode<StateT, ActT, P, N, 0>;
     if (smem > 48 * 1024) {

@@ -1,0 +1,69 @@
+"""Host-side checks of bench.py (no GPU): the algorithmic byte and flop counts, the profile
+parsing, and the N>1 aggregation on two gloo ranks."""
+import os
+import shutil
+
+import pytest
+
+import bench
+from recurrent_state_update_gb300 import workloads as wl
+
+
+def test_decode_algorithmic_bytes_per_token_layer():
+    # state read + write 2*H*P*N*2, conv state read + write 2*C_d*(W-1)*2, xBC in, z in, dt, y out
+    sh = wl.NEMOTRON_H_8B
+    assert sh.conv_dim == 10240
+    assert bench.DECODE_BYTES_PER_TOKEN_LAYER == 4_194_304 + 122_880 + 20_480 + 16_384 + 512 + 16_384 == 4_370_944
+    assert 256 * bench.DECODE_BYTES_PER_TOKEN_LAYER == 1_118_961_664
+
+
+def test_prefill_flop_count_one_chunk():
+    # one full 256-token chunk: C B^T per group (causal half), masked G X, chunk state, C h per head
+    L, H, P, N, G = 256, 128, 64, 128, 8
+    tri = L * (L + 1) / 2
+    want = G * tri * 2 * N + H * (tri * 2 * P + 4 * L * P * N)
+    assert bench.prefill_flops([256], 256) == pytest.approx(want)
+    assert bench.prefill_flops([300], 256) == pytest.approx(bench.prefill_flops([256], 256) + bench.prefill_flops([44], 256))
+
+
+def test_profile_traffic_is_dropped_when_the_kernel_source_changed(tmp_path, monkeypatch):
+    root = tmp_path
+    (root / "profiles").mkdir()
+    src = root / "k.cu"
+    src.write_text("kernel v1")
+    import hashlib
+    digest = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (root / "profiles" / "k.md").write_text(
+        f"# k\n\n- source: `k.cu`\n- source_sha256_16: `{digest}`\n- traffic_bytes_per_launch: `1234` (read + write)\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench._profile_traffic("k") == 1234.0
+    src.write_text("kernel v2")
+    assert bench._profile_traffic("k") is None
+    assert bench._profile_traffic("missing") is None
+
+
+def test_weak_scaling_value():
+    assert bench.weak_scaling_gbs(1_000_000_000, 4, 1000.0) == pytest.approx(4.0)
+
+
+def _rank_main(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [3.0, 7.5][rank]
+    got = bench._max_over_ranks(torch, dist, ms, device="cpu")
+    with open(os.path.join(out, f"r{rank}"), "w") as f:
+        f.write(repr(got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_on_two_gloo_ranks(tmp_path):
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    for r in range(2):
+        assert float((tmp_path / f"r{r}").read_text()) == 7.5
