@@ -16,7 +16,8 @@
 // 128-byte swizzle) and y is written: no per-chunk states travel through HBM.  The 256-token
 // chunks of the checkpoint grid are processed as two 128-token halves (the MMA M of one CTA);
 // the result is the same up to rounding.  Shared memory ~98 KB and 256 TMEM columns per CTA,
-// so two CTAs share an SM and cover each other's waits.  All waits are bounded.
+// so two CTAs share an SM and cover each other's waits; each CTA's eight warps split every
+// row's work in two.  All waits are bounded.
 #include <mutex>
 
 #include "common.cuh"
@@ -42,7 +43,7 @@ constexpr uint32_t OFF_C = 2 * BLK;    // C tile, rows i: [n 0..63 | n 64..127];
 constexpr uint32_t OFF_X = 4 * BLK;    // X tile, rows j, p 0..63; then w * X
 constexpr uint32_t OFF_H = 5 * BLK;    // h^T in bf16, rows n, p 0..63
 constexpr uint32_t OFF_SMALL = 6 * BLK;
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 2048 + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;  // + slack for the 1024-byte alignment
 
 struct Small {
     uint64_t bar_tma, bar_g, bar_yd, bar_s;
@@ -51,9 +52,10 @@ struct Small {
     float cum2[SQ];   // cum * log2(e)
     float delta[SQ];
     float w[SQ];
+    float ecol[SQ];  // column factors of the masked G
     float warp_tot[4];
 };
-static_assert(sizeof(Small) <= 2048, "small area");
+static_assert(sizeof(Small) <= 4096, "small area");
 
 constexpr uint32_t ID_G = idesc_bf16(128, 128, false, false);   // C (K-major) x B (K-major)
 constexpr uint32_t ID_YO = idesc_bf16(128, 64, false, true);    // C (K-major) x h^T (MN-major)
@@ -128,15 +130,21 @@ __global__ void __launch_bounds__(256) k_tc_meta(const ScanTcParams p) {
     if (tid == 0) p.meta[0] = 1;
 }
 
+// Threads: 8 warps.  Warp w works on TMEM lane quadrant q = w % 4 (rows 32q..32q+31 of every
+// accumulator) and on half hf = w / 4 of the columns, so each row's work is split over two warps.
+constexpr int kTcThreads = 256;
+
 template <typename StateT>
-__global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const __grid_constant__ CUtensorMap mX,
-                                                   const __grid_constant__ CUtensorMap mB,
-                                                   const __grid_constant__ CUtensorMap mC) {
+__global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, const __grid_constant__ CUtensorMap mX,
+                                                          const __grid_constant__ CUtensorMap mB,
+                                                          const __grid_constant__ CUtensorMap mC) {
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_smem) + 1023) &
                                                           ~static_cast<uintptr_t>(1023));
     Small *sv = reinterpret_cast<Small *>(sm + OFF_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, hf = warp >> 2;
+    const int row = q * 32 + lane;  // TMEM lane of this thread: token row i, or state row n
     if (p.meta[0] == 0) return;  // bad cu_seqlens (flagged): nothing is done
     const int s = p.meta[4 + blockIdx.x / p.H];
     const int h = blockIdx.x % p.H;
@@ -167,20 +175,18 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = sv->tmem;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t t_g = tm, t_yd = tm, t_yo = tm + 128, t_h = tm + 192;
+    const int c0 = hf * 32;  // this warp's 32 of the 64 head_dim columns
 
     // the stored state seeds the scan (chunked prefill hand-off): h^T into TMEM and its bf16 copy
     if (has_init) {
         const StateT *src = pool + (int64_t)slot * p.ssm_stride + head_off;
-        const int n = tid;
-        for (int c0 = 0; c0 < TP; c0 += 32) {
-            float v[32];
+        float v[32];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = to_f32(src[(int64_t)(c0 + q) * TN + n]);
-            tmem_st32(t_h + lane_base + c0, v);
-            store_hT_row(sm, n, v, c0);
-        }
+        for (int qq = 0; qq < 32; ++qq) v[qq] = to_f32(src[(int64_t)(c0 + qq) * TN + row]);
+        tmem_st32(t_h + lane_base + c0, v);
+        store_hT_row(sm, row, v, c0);
         fence_async_smem();
     }
     const int nsub = (len + SQ - 1) / SQ;
@@ -198,41 +204,42 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
     bool h_valid = has_init;
     bool failed = false;
     uint32_t ph = 0;
-    // dt of the sub-chunk about to run (prefetched one sub-chunk ahead)
+    // dt of the sub-chunk about to run (prefetched one sub-chunk ahead; thread = token)
     float dt_next = tid < min(SQ, len) ? load_scalar(p.dt, (int64_t)(t_begin + tid) * p.H + h, p.dt_bf16) : 0.0f;
     for (int k = 0; k < nsub; ++k, ph ^= 1u) {
         const int t0 = t_begin + k * SQ, L = min(SQ, len - k * SQ);
-        // the gate row of this thread's token, fetched now and used by the epilogue
-        uint4 zrow[8];
-        if (p.z && tid < L) {
+        // this thread's 32 gate values of its token row, fetched now and used by the epilogue
+        uint4 zrow[4];
+        if (p.z && row < L) {
             const uint4 *zr = reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(p.z) +
-                                                              ((int64_t)(t0 + tid) * p.H + h) * TP);
+                                                              ((int64_t)(t0 + row) * p.H + h) * TP + c0);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) zrow[q] = zr[q];
+            for (int qq = 0; qq < 4; ++qq) zrow[qq] = zr[qq];
         }
-        // Delta and the within-sub-chunk cumulative sum of Delta*A (thread = token)
-        float dlt = 0.0f;
-        if (tid < L) {
-            const float sdt = dt_next + bias;
-            dlt = p.dt_softplus ? softplus_f(sdt) : sdt;
-        }
-        {
+        // Delta and the within-sub-chunk cumulative sum of Delta*A (threads 0..127 = tokens)
+        float dlt = 0.0f, run = 0.0f;
+        if (tid < SQ) {
+            if (tid < L) {
+                const float sdt = dt_next + bias;
+                dlt = p.dt_softplus ? softplus_f(sdt) : sdt;
+            }
             const int Ln = min(SQ, len - (k + 1) * SQ);
-            dt_next = (k + 1 < nsub && tid < Ln)
-                          ? load_scalar(p.dt, (int64_t)(t0 + SQ + tid) * p.H + h, p.dt_bf16)
-                          : 0.0f;
-        }
-        float run = dlt * Ah;
+            dt_next = (k + 1 < nsub && tid < Ln) ? load_scalar(p.dt, (int64_t)(t0 + SQ + tid) * p.H + h, p.dt_bf16)
+                                                 : 0.0f;
+            run = dlt * Ah;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float v = __shfl_up_sync(0xffffffffu, run, off);
-            if (lane >= off) run += v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, run, off);
+                if (lane >= off) run += v;
+            }
+            if (lane == 31) sv->warp_tot[warp] = run;
         }
-        if (lane == 31) sv->warp_tot[warp] = run;
         __syncthreads();
-        for (int w2 = 0; w2 < warp; ++w2) run += sv->warp_tot[w2];
-        sv->cum2[tid] = run * LOG2E;
-        sv->delta[tid] = dlt;
+        if (tid < SQ) {
+            for (int w2 = 0; w2 < warp; ++w2) run += sv->warp_tot[w2];
+            sv->cum2[tid] = run * LOG2E;
+            sv->delta[tid] = dlt;
+        }
         // G = C B^T and Y_off = C h_prev^T
         int bad = 0;
         if (tid == 0) {
@@ -260,13 +267,24 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
             break;
         }
         const float cend = sv->cum2[L - 1];
-        sv->w[tid] = tid < L ? exp2f(cend - sv->cum2[tid]) * dlt : 0.0f;
-        // this thread's token row of X (for D x), read before the tile is scaled in place
-        uint4 xrow[8];
+        if (tid < SQ) {
+            // w_j = exp(cum_end - cum_j) Delta_j for the chunk state, and the column factor of the
+            // masked G: e_j = exp(cum_ref - cum_j) Delta_j with cum_ref the first column of j's
+            // 32-column block (exp(cum_i - cum_j) = exp(cum_i - cum_ref) e_j / Delta_j, both factors
+            // bounded for i >= j)
+            const float cj = sv->cum2[tid];
+            sv->w[tid] = tid < L ? exp2f(cend - cj) * dlt : 0.0f;
+            sv->ecol[tid] = tid < L ? exp2f(sv->cum2[tid & ~31] - cj) * dlt : 0.0f;
+        }
+        // this thread's 32 columns of its token row of X (for D x), read before the tile is scaled
+        uint4 xrow[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) xrow[q] = *reinterpret_cast<const uint4 *>(sm + OFF_X + swz128_chunk(tid, q));
+        for (int qq = 0; qq < 4; ++qq)
+            xrow[qq] = *reinterpret_cast<const uint4 *>(sm + OFF_X + swz128_chunk(row, hf * 4 + qq));
+        __syncthreads();  // ecol visible
 
-        // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, into the C buffer (C is consumed)
+        // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, written over the consumed C tile.
+        // Row i = this thread's lane; this warp forms column blocks jb = hf and hf + 2.
         bad = !mbar_wait(&sv->bar_g, ph, kPolls);
         if (__syncthreads_or(bad)) {
             failed = true;
@@ -275,31 +293,34 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
         if (tid == 0) pending &= ~2u;
         tc_fence_after();
         {
-            const int i = tid;
-            const float ci = sv->cum2[i];
-#pragma unroll 1
-            for (int jb = 0; jb < 4; ++jb) {
+            const float ci = sv->cum2[row];
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+                const int jb = hf + 2 * bb;
                 uint32_t pk[16];
-                if (jb <= warp) {  // warp-uniform: block jb holds columns j <= i for this warp's rows
+                if (jb <= q) {  // warp-uniform: block jb can hold columns j <= i for these rows
                     float gv[32];
                     tmem_ld32(t_g + lane_base + jb * 32, gv);
+                    const float rf = row < L ? exp2f(ci - sv->cum2[jb * 32]) : 0.0f;
+                    const float *ec = sv->ecol + jb * 32;
+                    if (jb < q) {
 #pragma unroll
-                    for (int q = 0; q < 32; q += 2) {
-                        const int j = jb * 32 + q;
-                        const float m0 = (j <= i && j < L && i < L) ? gv[q] * exp2f(ci - sv->cum2[j]) * sv->delta[j] : 0.0f;
-                        const float m1 = (j + 1 <= i && j + 1 < L && i < L)
-                                             ? gv[q + 1] * exp2f(ci - sv->cum2[j + 1]) * sv->delta[j + 1]
-                                             : 0.0f;
-                        pk[q / 2] = pack_bf16x2(m0, m1);
+                        for (int qq = 0; qq < 32; qq += 2)
+                            pk[qq / 2] = pack_bf16x2(gv[qq] * rf * ec[qq], gv[qq + 1] * rf * ec[qq + 1]);
+                    } else {  // diagonal block: j <= i
+#pragma unroll
+                        for (int qq = 0; qq < 32; qq += 2)
+                            pk[qq / 2] = pack_bf16x2(qq <= lane ? gv[qq] * rf * ec[qq] : 0.0f,
+                                                     qq + 1 <= lane ? gv[qq + 1] * rf * ec[qq + 1] : 0.0f);
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = 0u;
+                    for (int qq = 0; qq < 16; ++qq) pk[qq] = 0u;
                 }
                 unsigned char *blk = sm + OFF_C + (uint32_t)(jb >> 1) * BLK;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(blk + swz128_chunk(i, (jb & 1) * 4 + q4)) =
+                    *reinterpret_cast<uint4 *>(blk + swz128_chunk(row, (jb & 1) * 4 + q4)) =
                         make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
             }
         }
@@ -317,16 +338,14 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
             pending |= 4u;
             pend_par[2] = ph;
         }
-        // h^T <- exp(cum_end) h^T (thread = state row n)
+        // h^T <- exp(cum_end) h^T (lane = state row n, this warp's 32 head_dim columns)
         if (h_valid) {
             const float decay = exp2f(cend);
-            for (int c0 = 0; c0 < TP; c0 += 32) {
-                float v[32];
-                tmem_ld32(t_h + lane_base + c0, v);
+            float v[32];
+            tmem_ld32(t_h + lane_base + c0, v);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= decay;
-                tmem_st32(t_h + lane_base + c0, v);
-            }
+            for (int qq = 0; qq < 32; ++qq) v[qq] *= decay;
+            tmem_st32(t_h + lane_base + c0, v);
         }
         bad = !mbar_wait(&sv->bar_yd, ph, kPolls);
         if (__syncthreads_or(bad)) {
@@ -337,8 +356,8 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
         tc_fence_after();
         // w (.) X in place (the row of a 16-byte chunk is its byte offset / 128)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int cidx = tid + 128 * q;
+        for (int qq = 0; qq < 4; ++qq) {
+            const int cidx = tid + kTcThreads * qq;
             uint4 *ptr = reinterpret_cast<uint4 *>(sm + OFF_X + cidx * 16);
             const float wr = sv->w[cidx >> 3];
             uint4 u = *ptr;
@@ -365,45 +384,40 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
             pending |= 8u;
             pend_par[3] = ph;
         }
-        // y = Y_diag + exp(cum_i) Y_off + D x, gated by SiLU(z) (thread = token row i)
+        // y = Y_diag + exp(cum_i) Y_off + D x, gated by SiLU(z) (lane = token row i, 32 columns)
         {
-            const int i = tid;
-            const float ei = exp2f(sv->cum2[i]);
-            const int64_t row = ((int64_t)(t0 + i) * p.H + h) * TP;
-            const bool gate = p.z != nullptr;
-            bf16 *yr = static_cast<bf16 *>(p.y) + row;
+            const float ei = exp2f(sv->cum2[row]);
+            float yd[32], yo[32];
+            tmem_ld32(t_yd + lane_base + c0, yd);
+            if (h_valid) {
+                tmem_ld32(t_yo + lane_base + c0, yo);
+            } else {
 #pragma unroll
-            for (int c0 = 0; c0 < TP; c0 += 32) {
-                float yd[32], yo[32];
-                tmem_ld32(t_yd + lane_base + c0, yd);
-                if (h_valid) {
-                    tmem_ld32(t_yo + lane_base + c0, yo);
-                } else {
+                for (int qq = 0; qq < 32; ++qq) yo[qq] = 0.0f;
+            }
+            if (row < L) {
+                const bool gate = p.z != nullptr;
+                bf16 *yr = static_cast<bf16 *>(p.y) + ((int64_t)(t0 + row) * p.H + h) * TP + c0;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) yo[q] = 0.0f;
-                }
-                if (i < L) {
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const uint4 xv = xrow[q8];
+                    const uint4 zv = gate ? zrow[q8] : make_uint4(0, 0, 0, 0);
+                    const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv);
+                    const uint32_t *zw = reinterpret_cast<const uint32_t *>(&zv);
+                    uint4 out;
+                    uint32_t *ow = reinterpret_cast<uint32_t *>(&out);
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint4 xv = xrow[c0 / 8 + q8];
-                        const uint4 zv = gate ? zrow[c0 / 8 + q8] : make_uint4(0, 0, 0, 0);
-                        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv);
-                        const uint32_t *zw = reinterpret_cast<const uint32_t *>(&zv);
-                        uint4 out;
-                        uint32_t *ow = reinterpret_cast<uint32_t *>(&out);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int q = 8 * q8 + 2 * e;
-                            float v0 = yd[q] + ei * yo[q] + Dh * __uint_as_float(xw[e] << 16);
-                            float v1 = yd[q + 1] + ei * yo[q + 1] + Dh * __uint_as_float(xw[e] & 0xffff0000u);
-                            if (gate) {
-                                v0 *= silu_f(__uint_as_float(zw[e] << 16));
-                                v1 *= silu_f(__uint_as_float(zw[e] & 0xffff0000u));
-                            }
-                            ow[e] = pack_bf16x2(v0, v1);
+                    for (int e = 0; e < 4; ++e) {
+                        const int qq = 8 * q8 + 2 * e;
+                        float v0 = yd[qq] + ei * yo[qq] + Dh * __uint_as_float(xw[e] << 16);
+                        float v1 = yd[qq + 1] + ei * yo[qq + 1] + Dh * __uint_as_float(xw[e] & 0xffff0000u);
+                        if (gate) {
+                            v0 *= silu_f(__uint_as_float(zw[e] << 16));
+                            v1 *= silu_f(__uint_as_float(zw[e] & 0xffff0000u));
                         }
-                        *reinterpret_cast<uint4 *>(yr + c0 + 8 * q8) = out;
+                        ow[e] = pack_bf16x2(v0, v1);
                     }
+                    *reinterpret_cast<uint4 *>(yr + 8 * q8) = out;
                 }
             }
         }
@@ -425,7 +439,6 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
         }
         // h^T -> bf16 copy for the next C h^T; checkpoints and the final state -> pool
         {
-            const int n = tid;
             const int done = k * SQ + L;
             StateT *dst = nullptr;
             StateT *dst2 = nullptr;
@@ -441,13 +454,11 @@ __global__ void __launch_bounds__(128, 2) k_ssd_tc(const ScanTcParams p, const _
                 }
             }
             if (k == nsub - 1 && slot >= 0) dst2 = pool + (int64_t)slot * p.ssm_stride + head_off;
-            for (int c0 = 0; c0 < TP; c0 += 32) {
-                float v[32];
-                tmem_ld32(t_h + lane_base + c0, v);
-                if (k + 1 < nsub) store_hT_row(sm, n, v, c0);
-                if (dst) write_state(dst, n, v, c0);
-                if (dst2) write_state(dst2, n, v, c0);
-            }
+            float v[32];
+            tmem_ld32(t_h + lane_base + c0, v);
+            if (k + 1 < nsub) store_hT_row(sm, row, v, c0);
+            if (dst) write_state(dst, row, v, c0);
+            if (dst2) write_state(dst2, row, v, c0);
         }
         fence_async_smem();
         tc_fence_before();
@@ -523,7 +534,7 @@ int scan_tc_launch(const ScanTcParams &p, int state_bf16, cudaStream_t stream) {
     auto kern = state_bf16 ? k_ssd_tc<bf16> : k_ssd_tc<float>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
         return MAMBA_ECUDA;
-    kern<<<p.nseq * p.H, 128, SMEM_BYTES, stream>>>(p, mX, mB, mC);
+    kern<<<p.nseq * p.H, kTcThreads, SMEM_BYTES, stream>>>(p, mX, mB, mC);
     return launch_status();
 }
 
