@@ -343,10 +343,15 @@ def run_gpu(args):
     bld.build()
     hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
 
-    if args.only == "prefill":
-        prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
+    if args.only in ("prefill", "spec", "sweep"):
+        if args.only == "prefill":
+            res = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
+        elif args.only == "spec":
+            res = run_spec(torch, args, rank, dist, hbm_peak)
+        else:
+            res = run_sweep(torch, args, rank, dist, hbm_peak)
         if rank == 0:
-            print(json.dumps({"prefill": prefill}), flush=True)
+            print(json.dumps({args.only: res}), flush=True)
         if dist is not None:
             dist.destroy_process_group()
         return
@@ -376,9 +381,14 @@ def run_gpu(args):
                "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
     del dec
     torch.cuda.empty_cache()
-    prefill = None
+    prefill = spec = sweep = None
     if args.only == "all":
         prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
+        torch.cuda.empty_cache()
+        spec = run_spec(torch, args, rank, dist, hbm_peak)
+        torch.cuda.empty_cache()
+        sweep = run_sweep(torch, args, rank, dist, hbm_peak)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and args.only == "all" and not args.no_cpu_baseline:
@@ -386,9 +396,102 @@ def run_gpu(args):
 
     if rank == 0:
         emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck,
-             prefill, cpu)
+             prefill, cpu, spec, sweep)
     if dist is not None:
         dist.destroy_process_group()
+
+
+SPEC = wl.SPEC_DECODE
+SWEEP = wl.PADDING_SWEEP
+
+
+def spec_bytes(rows: int, accepted_rows: int, K: int, Wc: int) -> int:
+    """Algorithmic bytes of one speculative step (draft launch + commit) for `rows` requests:
+    draft: state read once, K states written to scratch, conv state read + written, K tokens of
+    xBC, z, y, dt; commit: the accepted rows copy one state (read + write) and every row re-seats
+    its conv state (read + write)."""
+    st = H * P * N * 2
+    conv = CD * Wc * 2
+    draft = rows * (st + K * st + 2 * conv + K * (CD * 2 + H * P * 2 * 2 + H * 4))
+    commit = accepted_rows * 2 * st + rows * 2 * conv
+    return draft + commit
+
+
+def run_spec(torch, args, rank, dist, hbm_peak):
+    """Speculative decode: batch 128, 4 draft tokens, 4 scratch slots per request, then the commit
+    of random accept lengths (one layer per step)."""
+    from recurrent_state_update_gb300 import binding as bd
+    dev = torch.device("cuda")
+    shape = SHAPE.with_spec(SPEC["ntok"])
+    batch, K = SPEC["batch"], SPEC["ntok"]
+    S = batch * (1 + K)
+    g = wl.rng(SPEC["seed"] * 1000 + rank, 0)
+    prm_np = wl.layer_params(g, shape)
+    prm = {k: torch.from_numpy(v).to(dev) for k, v in prm_np.items()}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SPEC["seed"] * 1000 + rank)
+    bf = torch.bfloat16
+    ssm = torch.randn(S, H, P, N, generator=gen, device=dev).mul_(0.1).to(bf)
+    conv = torch.randn(S, CD, shape.conv_cols, generator=gen, device=dev).mul_(0.1).to(bf)
+    ids = g.permutation(S).astype(np.int32)
+    slot = torch.from_numpy(ids[:batch]).to(dev)
+    scratch = torch.from_numpy(ids[batch:].reshape(batch, K).copy()).to(dev)
+    inp = wl.decode_inputs(g, shape, prm_np, batch, K, wl.BF16)
+    xbc = torch.from_numpy(inp["xbc"].view(np.int16)).to(dev).view(bf)
+    z = torch.from_numpy(inp["z"].view(np.int16)).to(dev).view(bf)
+    dt = torch.from_numpy(inp["dt"]).to(dev)
+    accept_np = wl.accept_lengths(g, batch, K)
+    accept = torch.from_numpy(accept_np).to(dev)
+    y = torch.empty(batch, K, H * P, dtype=bf, device=dev)
+    desc = bd.layer_desc(shape)
+
+    def step():
+        bd.mamba_state_update(desc, ssm, slot, xbc, dt, prm["A"], y, conv_pool=conv, conv_w=prm["conv_w"],
+                              scratch_slots=scratch, D=prm["D"], dt_bias=prm["dt_bias"], z=z)
+        bd.mamba_spec_commit(desc, ssm, slot, scratch, accept, conv_pool=conv)
+
+    ms = _max_over_ranks(torch, dist, _time(torch, step, max(args.steps, 10), max(args.warmup, 3), dist))
+    by = spec_bytes(batch, int((accept_np > 0).sum()), K, shape.conv_cols)
+    return {"workload": SPEC["name"], "ms_per_step": ms, "draft_tokens_per_s": batch * K / (ms * 1e-3),
+            "gbs": by / (ms * 1e-3) / 1e9, "hbm_frac": by / (ms * 1e-3) / 1e9 / hbm_peak,
+            "algorithmic_bytes": by, "launches_per_step": 2, "kernels": "k_decode (4 tokens), k_spec_commit"}
+
+
+def run_sweep(torch, args, rank, dist, hbm_peak):
+    """Decode at batch 1, 8, 64, 256, 1024 of a 1536-slot pool with 10 % of rows padded (-1):
+    per-launch time and GB/s over the non-padded rows (one layer)."""
+    from recurrent_state_update_gb300 import binding as bd
+    dev = torch.device("cuda")
+    bf = torch.bfloat16
+    pool = SWEEP["pool"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SWEEP["seed"] * 1000 + rank)
+    ssm = torch.randn(pool, H, P, N, generator=gen, device=dev).mul_(0.1).to(bf)
+    conv = torch.randn(pool, CD, W1, generator=gen, device=dev).mul_(0.1).to(bf)
+    g = wl.rng(SWEEP["seed"] * 1000 + rank, 0)
+    prm_np = wl.layer_params(g, SHAPE)
+    prm = {k: torch.from_numpy(v).to(dev) for k, v in prm_np.items()}
+    desc = bd.layer_desc(SHAPE)
+    out = []
+    for batch in SWEEP["batches"]:
+        ids = wl.slot_ids(g, pool, batch, SWEEP["pad_frac"])
+        live = int((ids >= 0).sum())
+        slot = torch.from_numpy(ids).to(dev)
+        inp = wl.decode_inputs(g, SHAPE, prm_np, batch, 1, wl.BF16)
+        xbc = torch.from_numpy(inp["xbc"].view(np.int16)).to(dev).view(bf)
+        z = torch.from_numpy(inp["z"].view(np.int16)).to(dev).view(bf)
+        dt = torch.from_numpy(inp["dt"]).to(dev)
+        y = torch.empty(batch, 1, H * P, dtype=bf, device=dev)
+
+        def step():
+            bd.mamba_state_update(desc, ssm, slot, xbc, dt, prm["A"], y, conv_pool=conv, conv_w=prm["conv_w"],
+                                  D=prm["D"], dt_bias=prm["dt_bias"], z=z)
+
+        ms = _max_over_ranks(torch, dist, _time(torch, step, max(args.steps, 20), max(args.warmup, 3), dist))
+        gbs = live * DECODE_BYTES_PER_TOKEN_LAYER / (ms * 1e-3) / 1e9
+        out.append({"batch": batch, "live_rows": live, "us_per_launch": ms * 1e3, "gbs": gbs,
+                    "hbm_frac": gbs / hbm_peak})
+    return {"workload": SWEEP["name"], "points": out}
 
 
 def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
@@ -411,7 +514,7 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
 
 
 def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
-     cpu):
+         cpu, spec=None, sweep=None):
     line = {
         "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -431,6 +534,8 @@ def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_
         "gpu_launches": args.steps * layers,
         "clocks": ck,
         "prefill": prefill,
+        "spec_decode": spec,
+        "padding_sweep": sweep,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -495,8 +600,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--layers", type=int, default=0, help="decode layers per step (default: the workload's 48)")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
-                    help="'decode' or 'prefill' times that form alone (profiling runs)")
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "spec", "sweep"], default="all",
+                    help="time one form alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
