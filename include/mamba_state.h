@@ -6,13 +6,13 @@
  *  [P1] "Hybrid SSM / Mamba models and non-KV state" (mlinterviewnotes.com):
  *       - the Mamba2 state shapes: conv state (d_conv, W-1+num_spec) with
  *         d_conv = d_inner + 2*n_groups*d_state, temporal state (nheads, head_dim, d_state);
- *       - the slot pool: one dense tensor per state object indexed [layer, slot, ...], plus a
- *         padding slot, requests holding an integer slot id;
+ *       - the slot pool: each state object is one tensor with a layer and a slot dimension,
+ *         plus one extra slot used for padding; a request owns an integer slot id;
  *       - the decode call selective_state_update(ssm_state, x, dt, A, B, C, D, z, dt_bias,
  *         dt_softplus, state_batch_indices, out);
  *       - the prefill call mamba_chunk_scan_combined(x viewed (1, T, H, P), dt, A, ...) and the
  *         chunked-prefill state hand-off (has_initial_states);
- *       - align-mode checkpoints "at position i * block_size";
+ *       - align-mode checkpoints: states kept at multiples of the block size;
  *       - the block-table "none"/"align" columns 1 + num_speculative_blocks (speculative
  *         decode keeps 1 + num_spec state pages per request).
  *  [P4] echobase "Mamba" notes, the Mamba block equations:
@@ -109,7 +109,7 @@ const char *mamba_status_string(int status);
 
 /*
  * mamba_conv_update -- causal depthwise conv1d + SiLU over ntok new tokens per request,
- * updating the conv state in place [P1 "a rolling window of the last W-1 token activations";
+ * updating the conv state in place [P1: the conv state keeps the most recent W-1 inputs;
  * P4 x = SiLU(Conv1d(x'))].
  *
  *   conv_pool        (num_slots, ...) with slot s at conv_pool + s*conv_slot_stride elements;
@@ -195,13 +195,14 @@ size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *desc, int32_t to
                                         int32_t nseq, int32_t chunk);
 
 /*
- * mamba_chunk_scan -- varlen chunked prefill in the SSD form [P1 mamba_chunk_scan_combined,
- * "masked matmul on tensor cores ... stitched with a small inter-chunk scan"; P4 Y = (M (.) L) X].
+ * mamba_chunk_scan -- varlen chunked prefill in the SSD form [P1 mamba_chunk_scan_combined: the
+ * within-chunk term as a masked matrix product on tensor cores, chunks joined by a short scan
+ * over chunk states; P4 Y = (M (.) L) X].
  * Sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]) of x; its tokens are split into
  * chunks of `chunk` tokens from its first token (the last chunk may be partial).  Per head:
  *     y_t = C_t . h_t + D*x_t  (then * SiLU(z_t) if z),  h_t = exp(Delta_t A) h_{t-1} + Delta_t x_t B_t^T
  * with h_{-1} = the state in slot_ids[s] when has_initial_state[s] != 0, else 0
- * [P1 chunked prefill is a state hand-off].  After the call slot_ids[s] holds the state after
+ * [P1: a later prefill chunk continues from the stored state].  After the call slot_ids[s] holds the state after
  * the sequence's last token; when ckpt_slots is given, ckpt_slots[s, k-1] (k >= 1, -1 = skip)
  * receives the state after the first k*ckpt_interval tokens of the sequence [P1 align mode:
  * states cached at positions i * block_size].

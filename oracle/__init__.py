@@ -10,7 +10,7 @@ Each wrapper names the passage of the pages the C function follows:
 
 * "Hybrid SSM / Mamba models and non-KV state" (mlinterviewnotes.com): state shapes,
   slot pool with a padding slot, the decode call with D / z / dt_bias / dt_softplus /
-  state_batch_indices, chunked prefill as a state hand-off, align-mode checkpoints, the
+  state_batch_indices, prefill chunks seeded from the stored state, align-mode checkpoints, the
   affine-composition snippet.
 * echobase "Mamba" notes: x = SiLU(Conv1d(x')), h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,
   y_t = C_t h_t (+ D x_t), y_hat = y * SiLU(z), and the SSD form Y = (M (.) L) X.
@@ -108,7 +108,7 @@ def conv_update(state, u, w, b=None):
 
     ``state`` is Cd x Wc (oldest column first) and is returned shifted by ntok with the new
     inputs appended.  Follows x = SiLU(Conv1d(x')) (echobase "Mamba" notes) and the conv
-    state as a rolling FIFO of the last W-1 inputs ("Hybrid SSM / Mamba models and non-KV
+    state as a FIFO holding the most recent W-1 inputs ("Hybrid SSM / Mamba models and non-KV
     state", the two-objects list).  Returns (new_state, out).
     """
     lib = _load()

@@ -382,7 +382,7 @@ static void steps_unit(int64_t unit, void *vctx) {
  * Varlen prefill by the step recurrence.  Sequence s owns tokens [cu[s], cu[s+1]).
  *   h0 (nullable): nseq x H x P x N initial states (zeros when NULL).
  *   x, z, y: T x H x P;  dt: T x H;  Bm, Cm: T x G x N.
- *   h_final: nseq x H x P x N, the state after the last token of each sequence.
+ *   h_final: nseq x H x P x N, each sequence's state once all its tokens are consumed.
  *   h_ckpt (nullable): nseq x max_ckpt x H x P x N; entry k-1 is the state after the
  *     first k*ckpt_interval tokens of the sequence (entries past the sequence untouched).
  */
@@ -504,7 +504,7 @@ int oracle_prefill_materialised(int H, int P, int N, int G, int T, const double 
  *   off-diagonal:    Y_i += exp(cum_i) C_i . h_prev
  *   chunk state:     S = sum_j exp(cum_end - cum_j) Delta_j x_j B_j^T
  *   state passing:   h = exp(cum_end) h_prev + S      (the affine composition across chunks)
- * This is the decomposition the intra-chunk masked matmul plus inter-chunk scan rests on.
+ * The tensor-core prefill computes exactly these four terms per chunk.
  */
 int oracle_prefill_chunked(int H, int P, int N, int G, int T, int Q, const double *h0,
                            const double *x, const double *dt, const double *A, const double *Bm,

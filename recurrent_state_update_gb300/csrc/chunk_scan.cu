@@ -1,8 +1,9 @@
 // chunk_scan.cu -- varlen chunked prefill of the Mamba2 state update in the SSD form.
 //
-// Operations ("Hybrid SSM / Mamba models and non-KV state": mamba_chunk_scan_combined, "the
-// intra-chunk contribution as a masked matmul ... stitched with a small inter-chunk scan",
-// chunked prefill as a state hand-off, align-mode checkpoints; echobase "Mamba" notes:
+// Operations ("Hybrid SSM / Mamba models and non-KV state": mamba_chunk_scan_combined, whose
+// within-chunk term is a masked matrix product and whose chunks are joined by a short scan over
+// chunk states; a later chunk continues from the stored state; align-mode checkpoints; echobase
+// "Mamba" notes:
 // y_i = sum_{j<=i} C_i (prod_{k=j+1..i} Abar_k) Bbar_j x_j, Y = (M (.) L) X):
 //   per chunk of Q tokens and head h, with cum_t = sum_{k<=t} Delta_k A_h inside the chunk:
 //     G     = C B^T                                       (per group, Q x Q)

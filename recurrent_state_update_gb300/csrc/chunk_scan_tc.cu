@@ -1,9 +1,9 @@
 // chunk_scan_tc.cu -- the chunked prefill (SSD form) on the tcgen05 tensor cores.
 //
-// Operations ("Hybrid SSM / Mamba models and non-KV state": mamba_chunk_scan_combined, "the
-// intra-chunk contribution as a masked matmul on tensor cores ... stitched with a small
-// inter-chunk scan", chunked prefill as a state hand-off, align-mode checkpoints; echobase
-// "Mamba" notes: Y = (M (.) L) X with M_ij = C_i (prod_{k=j+1..i} Abar_k) Bbar_j):
+// Operations ("Hybrid SSM / Mamba models and non-KV state": mamba_chunk_scan_combined, whose
+// within-chunk term is a masked matrix product on tensor cores and whose chunks are joined by a
+// short scan over chunk states; a later chunk continues from the stored state; align-mode
+// checkpoints; echobase "Mamba" notes: Y = (M (.) L) X with M_ij = C_i (prod_{k=j+1..i} Abar_k) Bbar_j):
 //   per sub-chunk of up to 128 tokens and head h, with cum_t = sum_{k<=t} Delta_k A_h:
 //     G     = C B^T                                         (tensor core, fp32 in TMEM)
 //     M     = G (.) exp(cum_i - cum_j) (.) Delta_j, j <= i   (CUDA cores, bf16 into shared memory)

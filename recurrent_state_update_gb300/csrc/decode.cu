@@ -874,8 +874,10 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     const size_t tile = (size_t)P * N * sizeof(StateT);
     const size_t rest = sizeof(float) * (size_t)decode_smem_floats(ntok, LC, a.HG, P, conv) +
                         (conv ? sizeof(ActT) * (size_t)LC * a.Wc : 0);
-    // two stages per head slot (up to 2 * nhs tiles in flight per CTA), fewer if shared memory is short
-    int sps = 2;
+    // two stages per head slot (up to 2 * nhs tiles in flight per CTA), fewer if shared memory is short;
+    // several tokens keep each tile in registers for a while, so one stage per slot suffices there and
+    // leaves room for two CTAs per SM
+    int sps = ntok > 1 ? 1 : 2;
     auto smem_for = [&](int k) { return decode_float_offset(k * nhs, tile) + rest; };
     while (sps > 1 && smem_for(sps) > 227 * 1024) --sps;
     const size_t smem = smem_for(sps);

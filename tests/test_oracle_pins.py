@@ -50,22 +50,25 @@ def _scalar_inputs(a_seq, b_seq):
     return dict(x=x, dt=delta.reshape(T, 1), A=np.array([-1.0]), B=ones, C=ones)
 
 
-def _compose(first, second):
-    # the page's composition rule: (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2)
-    a1, b1 = first
-    a2, b2 = second
-    return a2 * a1, a2 * b1 + b2
+def _affine_matrix(a, b):
+    """The step h -> a h + b as the 2x2 matrix acting on (h, 1)."""
+    return np.array([[a, b], [0.0, 1.0]])
 
 
 def test_affine_composition_page_example():
     g = _golden("affine_scan.txt")
     steps = [tuple(float(v) for v in s.split(",")) for s in g["steps"].split()]
-    left = _compose(_compose(steps[0], steps[1]), steps[2])
-    right = _compose(steps[0], _compose(steps[1], steps[2]))
-    np.testing.assert_allclose(left, right, rtol=1e-15)
+    m1, m2, m3 = (_affine_matrix(a, b) for a, b in steps)
+    # running step 1, then 2, then 3 is the product m3 m2 m1, grouped either way
+    grouped_late = m3 @ (m2 @ m1)
+    grouped_early = (m3 @ m2) @ m1
+    np.testing.assert_allclose(grouped_late, grouped_early, rtol=1e-15)
+    # two steps combined: slope a2 a1 and offset a2 b1 + b2, the rule the page states
+    (a1, b1), (a2, b2) = steps[0], steps[1]
+    np.testing.assert_allclose((m2 @ m1)[0], [a2 * a1, a2 * b1 + b2], rtol=1e-15)
     inp = _scalar_inputs([s[0] for s in steps], [s[1] for s in steps])
     for h0 in (0.0, 1.5, -3.0):
-        expect = left[0] * h0 + left[1]
+        expect = grouped_late[0, 0] * h0 + grouped_late[0, 1]
         # decode path, token by token
         h, y = oracle.ssm_update(np.full((1, 1, 1), h0), inp["x"], inp["B"], inp["C"], inp["dt"],
                                  inp["A"], dt_softplus=False)
@@ -101,10 +104,8 @@ def test_restored_error_propagates_by_factor_power(factor):
     he, ye = oracle.ssm_update(np.full((1, 1, 1), e0), x, ones, ones, dt, A, dt_softplus=False)
     hr, yr = oracle.ssm_update(np.full((1, 1, 1), r0), x, ones, ones, dt, A, dt_softplus=False)
     assert hr[0, 0, 0] - he[0, 0, 0] == pytest.approx((r0 - e0) * factor ** n, rel=1e-9)
-    # the page's own loop for the exact trajectory
-    exact = e0
-    for _ in range(n):
-        exact = factor * exact + inc
+    # closed form of n steps of h <- factor h + inc: factor^n h0 + inc (factor^n - 1) / (factor - 1)
+    exact = factor ** n * e0 + inc * (factor ** n - 1.0) / (factor - 1.0)
     assert he[0, 0, 0] == pytest.approx(exact, rel=1e-12)
 
 
