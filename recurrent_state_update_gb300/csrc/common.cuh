@@ -66,6 +66,10 @@ struct Vec16 {
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
+// SiLU with the fast exponential and divide intrinsics (a few ulp; for large negative v the
+// divide by an infinite denominator gives 0, the limit).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+
 // softplus in fp32: log(1 + e^s), with the linear branch above 20 (the tail below the branch
 // point differs from s by less than e^-20 relative).
 __device__ __forceinline__ float softplus_f(float s) { return s > 20.0f ? s : log1pf(expf(s)); }

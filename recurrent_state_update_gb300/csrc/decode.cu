@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
 // the copies still in flight are drained (bounded) before the CTA exits.
 
 constexpr int kStreamConsumers = 256;  // consumer threads (head slots of TH threads)
-constexpr int kStreamConv = 64;        // conv threads
+constexpr int kStreamConv = 128;       // conv threads
 constexpr int kStreamThreads = kStreamConsumers + kStreamConv + 32;
 
 struct StreamArgs {
@@ -418,26 +418,40 @@ struct StreamArgs {
     int ns;  // tile stages
 };
 
-// per-item buffer: xs[LC] | dl[HG] | da[HG] | zf[HG*P] | ys[HG*P]   (floats), rounded up to 16 bytes so
-// that both buffers keep the float4 alignment of xs
-__host__ __device__ inline int stream_item_floats(int LC, int HG, int P) {
-    return (LC + 2 * HG + 2 * HG * P + 3) & ~3;
-}
-
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
-// Shared-memory map of the stream kernel (byte offsets).
+// Per-item buffer (byte offsets): xs[LC] | dl[HG] | da[HG] floats, the raw z row (ActT), ys[HG*P]
+// floats; every part 16-byte aligned.
+struct ItemLayout {
+    size_t dl, da, zr, ys, bytes;
+    __host__ __device__ ItemLayout(int LC, int HG, int P, size_t es) {
+        dl = sizeof(float) * (size_t)LC;
+        da = dl + sizeof(float) * (size_t)HG;
+        zr = align16(da + sizeof(float) * (size_t)HG);
+        ys = align16(zr + es * (size_t)HG * P);
+        bytes = align16(ys + sizeof(float) * (size_t)HG * P);
+    }
+};
+
+// Shared-memory map of the stream kernel (byte offsets).  The conv inputs of an item (old conv
+// state, raw xBC, z row, dt slice) are double-buffered so the next item's copies overlap this one.
 struct StreamSmem {
-    size_t bars, flags, items, wsm, cs, ur, zr, total;
-    __host__ __device__ StreamSmem(int ns, size_t tile, int LC, int HG, int P, int W, int Wc, size_t es) {
-        bars = (size_t)ns * tile;                       // stages first (16-byte aligned tiles)
-        flags = align16(bars + 8 * (size_t)(2 * ns + 7));  // full/empty, xs_full/empty, cons, conv, conv_in
-        items = flags + 16;                             // abort, issued, cached tap group
-        wsm = items + sizeof(float) * 2 * (size_t)stream_item_floats(LC, HG, P);
-        cs = align16(wsm + sizeof(float) * (size_t)LC * W);  // conv taps of the cached group
-        ur = align16(cs + es * (size_t)LC * Wc);        // old conv state of the item
-        zr = align16(ur + es * (size_t)LC);             // raw inputs of the item
-        total = align16(zr + es * (size_t)HG * P);      // z row of the item
+    size_t bars, flags, items, item_bytes, wsm, ga, gb, in0, in_bytes, cs, ur, zin, dts, total;
+    __host__ __device__ StreamSmem(int ns, size_t tile, int LC, int HG, int P, int W, int Wc, size_t es, size_t dt_es) {
+        bars = (size_t)ns * tile;                          // stages first (16-byte aligned tiles)
+        flags = align16(bars + 8 * (size_t)(2 * ns + 8));  // full/empty, xs_full/empty, cons, conv, conv_in[2]
+        items = flags + 16;                                // abort, issued
+        item_bytes = ItemLayout(LC, HG, P, es).bytes;
+        wsm = items + 2 * item_bytes;                      // conv taps of the cached group
+        ga = align16(wsm + sizeof(float) * (size_t)LC * W);  // A of the cached group's heads
+        gb = align16(ga + sizeof(float) * (size_t)HG);     // dt_bias of the cached group's heads
+        in0 = align16(gb + sizeof(float) * (size_t)HG);
+        cs = 0;                                            // offsets inside one input buffer:
+        ur = align16(cs + es * (size_t)LC * Wc);           //   old conv state, raw xBC,
+        zin = align16(ur + es * (size_t)LC);               //   z row,
+        dts = align16(zin + es * (size_t)HG * P);          //   dt slice
+        in_bytes = align16(dts + dt_es * (size_t)HG);
+        total = in0 + 2 * in_bytes;
     }
 };
 
@@ -484,7 +498,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
     const int HP = a.H * P, GN = a.G * N;
     const int tid = threadIdx.x;
     const int W = a.batch * G;
-    const StreamSmem L(NS, TILE_BYTES, LC, HG, P, Wk, Wc, ES);
+    const size_t DTES = a.dt_bf16 ? 2 : 4;
+    const StreamSmem L(NS, TILE_BYTES, LC, HG, P, Wk, Wc, ES, DTES);
 
     extern __shared__ __align__(128) unsigned char st_smem[];
     unsigned char *stages = st_smem;
@@ -494,15 +509,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
     uint64_t *xs_empty = xs_full + 2;  // [2]
     uint64_t *cons_bar = xs_empty + 2;
     uint64_t *conv_bar = cons_bar + 1;
-    uint64_t *conv_in = conv_bar + 1;
+    uint64_t *conv_in = conv_bar + 1;  // [2]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(st_smem + L.flags);
     int *issued = reinterpret_cast<int *>(st_smem + L.flags) + 1;  // tiles issued by the producer
-    float *items = reinterpret_cast<float *>(st_smem + L.items);
-    const int IF = stream_item_floats(LC, HG, P);
+    const ItemLayout IL(LC, HG, P, ES);
+    auto item = [&](int e) { return st_smem + L.items + (size_t)e * L.item_bytes; };
     float *wsm = reinterpret_cast<float *>(st_smem + L.wsm);
-    ActT *cs = reinterpret_cast<ActT *>(st_smem + L.cs);
-    ActT *ur = reinterpret_cast<ActT *>(st_smem + L.ur);
-    ActT *zr = reinterpret_cast<ActT *>(st_smem + L.zr);
+    float *gA = reinterpret_cast<float *>(st_smem + L.ga);
+    float *gBias = reinterpret_cast<float *>(st_smem + L.gb);
+    auto inbuf = [&](int b) { return st_smem + L.in0 + (size_t)b * L.in_bytes; };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -515,7 +530,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
         }
         umma::mbar_init(cons_bar, kStreamConsumers);
         umma::mbar_init(conv_bar, kStreamConv);
-        umma::mbar_init(conv_in, 1);
+        umma::mbar_init(&conv_in[0], 1);
+        umma::mbar_init(&conv_in[1], 1);
         umma::fence_mbar_init();
         *abort_flag = 0;
         *issued = 0;
@@ -549,89 +565,128 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
         }
     } else if (tid >= kStreamConsumers) {
         // ---------------- conv warps ----------------
-        // the item's inputs arrive by bulk copies (conv state and xBC of the group's channels in
-        // the order x | B | C, the z row, and the group's conv taps when the group changes)
+        // An item's conv inputs arrive by bulk copies into one of two input buffers: the next
+        // item's copies are issued while this item is convolved.  The conv taps, A and dt_bias of
+        // the item's group are cached and reloaded only when the group changes.
         const int ct = tid - kStreamConsumers;
-        uint32_t cph = 0, iph = 0;
-        int n = 0, wgroup = -1;
-        const size_t xseg = (size_t)HG * P, bseg = N;  // channels per segment
-        for (int w = blockIdx.x; w < W; w += gridDim.x) {
-            const int32_t s = item_slot(w);
-            if (s < 0) continue;
-            const int e = n & 1;
-            if (n >= 2 && !stream_wait(&xs_empty[e], (uint32_t)(n / 2 - 1) & 1u, abort_flag)) break;
-            if (*abort_flag) break;
+        const size_t xseg = (size_t)HG * P, bseg = N;  // channels per segment: x | B | C
+        auto next_valid = [&](int w) {
+            while (w < W && item_slot(w) < 0) {
+                if (ct == 0 && w % G == 0 && a.slot[w / G] >= a.num_slots) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+                w += gridDim.x;
+            }
+            return w;
+        };
+        // issue the conv inputs of item w into input buffer b (and the group's parameters)
+        auto issue_inputs = [&](int w, int b, bool params) {
             const int i = w / G, g = w % G;
+            const int32_t s = item_slot(w);
             const int lo[3] = {g * HG * P, HP + g * N, HP + GN + g * N};
             const size_t len[3] = {xseg, bseg, bseg};
-            if (ct == 0) {
-                uint32_t bytes = (uint32_t)((size_t)LC * Wc * ES + (size_t)LC * ES + (a.z ? (size_t)HG * P * ES : 0));
-                if (wgroup != g) bytes += (uint32_t)(sizeof(float) * (size_t)LC * Wk);
-                umma::fence_async_smem();
-                umma::mbar_arrive_expect_tx(conv_in, bytes);
-                const ActT *cstate = static_cast<const ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
-                const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * a.Cd;
-                size_t base = 0;
-                for (int r = 0; r < 3; ++r) {
-                    bulk_copy(cs + base * Wc, cstate + (int64_t)lo[r] * Wc, (uint32_t)(len[r] * Wc * ES), conv_in);
-                    bulk_copy(ur + base, u_row + lo[r], (uint32_t)(len[r] * ES), conv_in);
-                    if (wgroup != g)
-                        bulk_copy(wsm + base * Wk, a.conv_w + (int64_t)lo[r] * Wk, (uint32_t)(len[r] * Wk * sizeof(float)),
-                                  conv_in);
-                    base += len[r];
-                }
-                if (a.z)
-                    bulk_copy(zr, static_cast<const ActT *>(a.z) + (int64_t)i * HP + (int64_t)g * HG * P,
-                              (uint32_t)((size_t)HG * P * ES), conv_in);
+            unsigned char *ib = inbuf(b);
+            uint32_t bytes = (uint32_t)((size_t)LC * Wc * ES + (size_t)LC * ES + (a.z ? (size_t)HG * P * ES : 0) +
+                                        (size_t)HG * DTES);
+            if (params) bytes += (uint32_t)(sizeof(float) * ((size_t)LC * Wk + HG + (a.dt_bias ? HG : 0)));
+            umma::fence_async_smem();
+            umma::mbar_arrive_expect_tx(&conv_in[b], bytes);
+            const ActT *cstate = static_cast<const ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+            const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * a.Cd;
+            size_t base = 0;
+            for (int r = 0; r < 3; ++r) {
+                bulk_copy(reinterpret_cast<ActT *>(ib + L.cs) + base * Wc, cstate + (int64_t)lo[r] * Wc,
+                          (uint32_t)(len[r] * Wc * ES), &conv_in[b]);
+                bulk_copy(reinterpret_cast<ActT *>(ib + L.ur) + base, u_row + lo[r], (uint32_t)(len[r] * ES), &conv_in[b]);
+                if (params)
+                    bulk_copy(wsm + base * Wk, a.conv_w + (int64_t)lo[r] * Wk, (uint32_t)(len[r] * Wk * sizeof(float)),
+                              &conv_in[b]);
+                base += len[r];
             }
-            wgroup = g;
-            if (!stream_wait(conv_in, iph & 1u, abort_flag)) break;
-            ++iph;
-            float *xs = items + e * IF, *dl = xs + LC, *da = dl + HG, *zf = da + HG;
+            if (a.z)
+                bulk_copy(ib + L.zin, static_cast<const ActT *>(a.z) + (int64_t)i * HP + (int64_t)g * HG * P,
+                          (uint32_t)((size_t)HG * P * ES), &conv_in[b]);
+            bulk_copy(ib + L.dts, static_cast<const unsigned char *>(a.dt) + ((int64_t)i * a.H + (int64_t)g * HG) * DTES,
+                      (uint32_t)(HG * DTES), &conv_in[b]);
+            if (params) {
+                bulk_copy(gA, a.A + (int64_t)g * HG, (uint32_t)(HG * sizeof(float)), &conv_in[b]);
+                if (a.dt_bias) bulk_copy(gBias, a.dt_bias + (int64_t)g * HG, (uint32_t)(HG * sizeof(float)), &conv_in[b]);
+            }
+        };
+        uint32_t cph = 0, iph[2] = {0u, 0u}, issued_in[2] = {0u, 0u};
+        int n = 0;
+        int w = next_valid(blockIdx.x);
+        if (ct == 0 && w < W) {
+            issue_inputs(w, 0, true);
+            ++issued_in[0];
+        }
+        while (w < W) {
+            const int b = n & 1, e = n & 1;
+            const int g = w % G, i = w / G;
+            const int wn = next_valid(w + gridDim.x);
+            const bool same_group = wn < W && wn % G == g;
+            if (ct == 0 && same_group) {  // overlaps this item
+                issue_inputs(wn, b ^ 1, false);
+                ++issued_in[b ^ 1];
+            }
+            if (n >= 2 && !stream_wait(&xs_empty[e], (uint32_t)(n / 2 - 1) & 1u, abort_flag)) break;
+            if (!stream_wait(&conv_in[b], iph[b] & 1u, abort_flag)) break;
+            ++iph[b];
+            const int32_t s = item_slot(w);
+            const int lo[3] = {g * HG * P, HP + g * N, HP + GN + g * N};
+            unsigned char *ib = inbuf(b), *it = item(e);
+            const ActT *cs = reinterpret_cast<const ActT *>(ib + L.cs);
+            const ActT *ur = reinterpret_cast<const ActT *>(ib + L.ur);
+            float *xs = reinterpret_cast<float *>(it), *dl = reinterpret_cast<float *>(it + IL.dl),
+                  *da = reinterpret_cast<float *>(it + IL.da);
+            ActT *cstate = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+            // conv + SiLU per channel; the channel's shifted window goes straight back to the pool
             for (int lc = ct; lc < LC; lc += kStreamConv) {
                 const int r = lc < (int)xseg ? 0 : (lc < (int)(xseg + bseg) ? 1 : 2);
                 const int c = lo[r] + lc - (r == 0 ? 0 : (r == 1 ? (int)xseg : (int)(xseg + bseg)));
                 float v = a.conv_b ? a.conv_b[c] : 0.0f;
-                for (int k = 0; k < Wk; ++k) {
-                    const int m = Wc - (Wk - 1) + k;
-                    const float val = m < Wc ? to_f32(cs[lc * Wc + m]) : to_f32(ur[lc]);
-                    v = fmaf(wsm[lc * Wk + k], val, v);
+                const ActT *win = cs + lc * Wc;
+                const ActT u = ur[lc];
+                if (Wk == 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(wsm + lc * 4);
+                    v = fmaf(w4.x, to_f32(win[Wc - 3]), v);
+                    v = fmaf(w4.y, to_f32(win[Wc - 2]), v);
+                    v = fmaf(w4.z, to_f32(win[Wc - 1]), v);
+                    v = fmaf(w4.w, to_f32(u), v);
+                } else {
+                    for (int k = 0; k < Wk; ++k) {
+                        const int m = Wc - (Wk - 1) + k;
+                        v = fmaf(wsm[lc * Wk + k], to_f32(m < Wc ? win[m] : u), v);
+                    }
                 }
-                xs[lc] = silu_f(v);
+                xs[lc] = silu_fast(v);
+                ActT *nw = cstate + (int64_t)c * Wc;
+                for (int k = 0; k + 1 < Wc; ++k) nw[k] = win[k + 1];
+                nw[Wc - 1] = u;
+            }
+            if (a.z) {
+                const uint4 *zsrc = reinterpret_cast<const uint4 *>(ib + L.zin);
+                uint4 *zdst = reinterpret_cast<uint4 *>(it + IL.zr);
+                for (int q = ct; q < (int)((size_t)HG * P * ES / 16); q += kStreamConv) zdst[q] = zsrc[q];
             }
             for (int hl = ct; hl < HG; hl += kStreamConv) {
-                const int h = g * HG + hl;
-                const float sdt = load_scalar(a.dt, (int64_t)i * a.H + h, a.dt_bf16) + (a.dt_bias ? a.dt_bias[h] : 0.0f);
+                const float sdt = load_scalar(ib + L.dts, hl, a.dt_bf16) + (a.dt_bias ? gBias[hl] : 0.0f);
                 const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
                 dl[hl] = delta;
-                da[hl] = expf(delta * a.A[h]);
-            }
-            if (a.z)
-                for (int q = ct; q < HG * P; q += kStreamConv) zf[q] = to_f32(zr[q]);
-            // the shifted conv state, 16 bytes per store: new column k is old column k+1, the last is the input
-            {
-                ActT *cstate = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
-                constexpr int VE = 16 / ES;
-                size_t base = 0;
-                for (int r = 0; r < 3; ++r) {
-                    const int nv = (int)(len[r] * Wc / VE);
-                    uint4 *dst = reinterpret_cast<uint4 *>(cstate + (int64_t)lo[r] * Wc);
-                    for (int v = ct; v < nv; v += kStreamConv) {
-                        ActT out[VE];
-#pragma unroll
-                        for (int q = 0; q < VE; ++q) {
-                            const int el = v * VE + q, lcl = el / Wc, k = el - lcl * Wc;
-                            out[q] = k + 1 < Wc ? cs[(base + lcl) * Wc + k + 1] : ur[base + lcl];
-                        }
-                        dst[v] = *reinterpret_cast<const uint4 *>(out);
-                    }
-                    base += len[r];
-                }
+                da[hl] = expf(delta * gA[hl]);
             }
             mbar_arrive(&xs_full[e]);
-            if (!group_sync(conv_bar, cph, abort_flag)) break;  // cs / ur / zr / taps are refilled next
+            if (!group_sync(conv_bar, cph, abort_flag)) break;  // buffer b and the taps are no longer read
+            if (ct == 0 && wn < W && !same_group) {
+                issue_inputs(wn, b ^ 1, true);
+                ++issued_in[b ^ 1];
+            }
+            (void)i;
+            w = wn;
             ++n;
         }
+        // after an abort, input copies this role issued may still be landing: wait for them (bounded)
+        if (ct == 0)
+            for (int b = 0; b < 2; ++b)
+                if (issued_in[b] > iph[b]) umma::mbar_wait(&conv_in[b], iph[b] & 1u, kMaxPolls);
     } else {
         // ---------------- consumer warps ----------------
         const int hs = tid / TH, th = tid - hs * TH, lane = tid & 31;
@@ -644,7 +699,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
             const int e = n & 1;
             if (!stream_wait(&xs_full[e], (uint32_t)(n / 2) & 1u, abort_flag)) break;
             const int i = w / G, g = w % G;
-            float *xs = items + e * IF, *dl = xs + LC, *da = dl + HG, *zf = da + HG, *ys = zf + HG * P;
+            unsigned char *it = item(e);
+            const float *xs = reinterpret_cast<const float *>(it), *dl = reinterpret_cast<const float *>(it + IL.dl),
+                        *da = reinterpret_cast<const float *>(it + IL.da);
+            const ActT *zraw = reinterpret_cast<const ActT *>(it + IL.zr);
+            float *ys = reinterpret_cast<float *>(it + IL.ys);
             StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
             float Bv[VEC], Cv[VEC];
 #pragma unroll
@@ -656,6 +715,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
             }
             bool stop = false;
             for (int hl = hs; hl < HG; hl += NHS) {
+                // stage st only ever holds this slot's tiles (the host sizes NS for that), so the
+                // phase before t / NS is one this slot has already consumed
                 const int t = t0 + hl, st = t % NS;
                 if (!stream_wait(&full[st], (uint32_t)(t / NS) & 1u, abort_flag)) {
                     stop = true;
@@ -694,7 +755,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
                 const int h = g * HG + q / P;
                 const float xv = xs[q];
                 float yv = ys[q] + (a.D ? a.D[h] * xv : 0.0f);
-                if (a.z) yv *= silu_f(zf[q]);
+                if (a.z) yv *= silu_fast(to_f32(zraw[q]));
                 yr[q] = from_f32<ActT>(yv);
             }
             mbar_arrive(&xs_empty[e]);
@@ -708,8 +769,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
         flag_error(a.err, MAMBA_ERR_TIMEOUT);
         const int ti = *issued;
         for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t) umma::mbar_wait(&full[t % NS], (uint32_t)(t / NS) & 1u, kMaxPolls);
-        umma::mbar_wait(conv_in, 0u, 1024);
-        umma::mbar_wait(conv_in, 1u, 1024);
+
     }
 }
 
@@ -828,7 +888,7 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 template <typename StateT, typename ActT, int P, int N>
 static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int LC = a.HG * P + 2 * N;
-    const size_t es = sizeof(ActT), tile = (size_t)P * N * sizeof(StateT);
+    const size_t es = sizeof(ActT), tile = (size_t)P * N * sizeof(StateT), dt_es = a.dt_bf16 ? 2 : 4;
     const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N, HGP = (size_t)a.HG * P;
     auto a16 = [](size_t v) { return v % 16 == 0; };
     auto p16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
@@ -836,11 +896,21 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
                          a16((size_t)a.conv_stride * es) && a16(HGP * a.Wc * es) && a16((size_t)N * a.Wc * es) &&
                          a16(HP * a.Wc * es) && a16(GN * a.Wc * es) && a16((size_t)a.Cd * es) && a16(HGP * es) &&
                          a16((size_t)N * es) && a16(HP * es) && a16(GN * es) && a16(HGP * a.W * 4) &&
-                         a16((size_t)N * a.W * 4) && a16(HP * a.W * 4) && a16(GN * a.W * 4);
+                         a16((size_t)N * a.W * 4) && a16(HP * a.W * 4) && a16(GN * a.W * 4) && p16(a.dt) &&
+                         p16(a.A) && (!a.dt_bias || p16(a.dt_bias)) && a16((size_t)a.HG * dt_es) &&
+                         a16((size_t)a.H * dt_es) && a16((size_t)a.HG * 4);
     if (!aligned) return 1;
-    int ns = 16;
-    while (ns > 2 && StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es).total > 220 * 1024) --ns;
-    const size_t smem = StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es).total;
+    // Stage ownership: tile t goes to stage t % ns and to head slot (t % HG) % NHS.  A stage must
+    // always serve the same head slot (slot(t) == slot(t - ns)); otherwise a slot that runs ahead
+    // could wait on a stage whose previous phase belongs to the other slot and is still pending,
+    // and a parity wait cannot tell the two phases apart.  So ns is a multiple of NHS when NHS
+    // divides HG, and a multiple of HG otherwise.
+    constexpr int NHS = kStreamConsumers / Tile<StateT, P, N>::TH;
+    const int step = (a.HG % NHS == 0) ? NHS : a.HG;
+    int ns = 16 - 16 % step;
+    while (ns > step && StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total > 220 * 1024) ns -= step;
+    if (ns < step || ns % step != 0) return 1;
+    const size_t smem = StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total;
     if (smem > 227 * 1024) return 1;
     static int sm_count = 0;
     if (sm_count == 0) {
