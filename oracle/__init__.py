@@ -63,6 +63,9 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_spec_commit.argtypes = [i64, i32, i32, i32, i32, _dp, i64, _dp, i64, _ip, _ip, _ip]
         lib.oracle_spec_commit.restype = i32
+        lib.oracle_conv_varlen.argtypes = [i32, i32, i32, i32, _ip, ctypes.POINTER(ctypes.c_uint8), _dp,
+                                           _dp, _dp, _dp, _dp]
+        lib.oracle_conv_varlen.restype = i32
         lib.oracle_prefill_steps.argtypes = [i32, i32, i32, i32, i32, _ip, _dp, _dp, _dp, _dp, _dp,
                                              _dp, _dp, _dp, i32, _dp, _dp, _dp, i32, i32, _dp, i32]
         lib.oracle_prefill_steps.restype = i32
@@ -202,6 +205,38 @@ def spec_commit(ssm_pool, slot, scratch, accept, *, conv_pool=None):
 # --------------------------------------------------------------------------------------
 # prefill
 # --------------------------------------------------------------------------------------
+
+def conv_varlen(cu_seqlens, u, w, b=None, *, state=None, init=None):
+    """Varlen causal conv1d + SiLU of a prefill batch, with the conv state carried in and out.
+
+    Follows x = SiLU(Conv1d(x')) (echobase "Mamba" notes) applied to whole prompts, with the
+    conv state as the window of the most recent inputs that a later chunk continues from
+    ("Hybrid SSM / Mamba models and non-KV state": the conv state object and the chunked-prefill
+    hand-off).  u: T x Cd raw inputs; w: Cd x W; state: nseq x Cd x Wc (oldest first) or None
+    (zeros, Wc = W-1); init: nseq flags (None = no sequence starts from its state).
+    Returns (new_state, out) with out T x Cd.
+    """
+    lib = _load()
+    u = _f64(u)
+    T, Cd = u.shape
+    w = _f64(w)
+    W = w.shape[1]
+    cu = _i32(cu_seqlens)
+    nseq = cu.shape[0] - 1
+    if state is None:
+        st = np.zeros((nseq, Cd, W - 1), np.float64)
+    else:
+        st = _f64(state).copy()
+    Wc = st.shape[2]
+    flags = None if init is None else np.ascontiguousarray(init, dtype=np.uint8)
+    out = np.full((T, Cd), np.nan)
+    rc = lib.oracle_conv_varlen(Cd, Wc, W, nseq, _pi(cu),
+                                None if flags is None else flags.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                                _p(st), _p(u), _p(w), _p(_f64(b)), _p(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv_varlen failed: {rc}")
+    return st, out
+
 
 def prefill_steps(cu_seqlens, x, dt, A, B, C, *, h0=None, D=None, dt_bias=None, dt_softplus=True,
                   z=None, ckpt_interval=0, max_ckpt=0, nthreads=None):

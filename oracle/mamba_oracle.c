@@ -323,6 +323,57 @@ int oracle_spec_commit(int64_t ssm_elems, int Cd, int Wc, int ntok, int batch, d
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* prefill: varlen causal conv1d + SiLU, conv state read at the start and written back   */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * The conv in front of the chunked scan (x = SiLU(Conv1d(x')) of the Mamba block, applied to a
+ * whole prompt; the conv state as the FIFO of the most recent inputs, continued across prefill
+ * chunks like the temporal state).  Sequence s owns rows [cu[s], cu[s+1]) of u (T x Cd raw
+ * inputs).  Its input stream is e_s(q) for q = -Wc .. L-1:
+ *     e_s(q) = state[s, c, Wc + q]   for q < 0 when init[s] != 0 (zero when init[s] == 0),
+ *     e_s(q) = u[cu[s] + q, c]       for q >= 0.
+ * Token q of the sequence convolves the W inputs ending at itself:
+ *     out[cu[s] + q, c] = SiLU(b_c + sum_{k=0..W-1} w[c, k] * e_s(q - (W-1) + k)).
+ * On return state[s, c, i] = e_s(L - Wc + i) for i = 0..Wc-1: the last Wc inputs of the
+ * stream (for L >= Wc only new inputs; an empty sequence keeps its old window, or zeros).
+ *   state: nseq x Cd x Wc (oldest column first), w: Cd x W, b: Cd or NULL, out: T x Cd.
+ *   init: nseq bytes or NULL (all zero).
+ */
+int oracle_conv_varlen(int Cd, int Wc, int W, int nseq, const int32_t *cu, const uint8_t *init,
+                       double *state, const double *u, const double *w, const double *b,
+                       double *out) {
+    if (Cd <= 0 || W < 1 || Wc < W - 1 || nseq < 0) return OR_EINVAL;
+    for (int s = 0; s < nseq; ++s)
+        if (cu[s + 1] < cu[s]) return OR_EINVAL;
+    double *stream = NULL;
+    for (int s = 0; s < nseq; ++s) {
+        const int L = cu[s + 1] - cu[s];
+        const int has = init ? init[s] != 0 : 0;
+        double *ns = (double *)realloc(stream, sizeof(double) * (size_t)(Wc + L));
+        if (!ns) {
+            free(stream);
+            return OR_ENOMEM;
+        }
+        stream = ns;
+        for (int c = 0; c < Cd; ++c) {
+            double *st = state + ((int64_t)s * Cd + c) * Wc;
+            /* stream[Wc + q] = e_s(q) */
+            for (int i = 0; i < Wc; ++i) stream[i] = has ? st[i] : 0.0;
+            for (int q = 0; q < L; ++q) stream[Wc + q] = u[((int64_t)cu[s] + q) * Cd + c];
+            for (int q = 0; q < L; ++q) {
+                double v = b ? b[c] : 0.0;
+                for (int k = 0; k < W; ++k) v += w[(int64_t)c * W + k] * stream[Wc + q - (W - 1) + k];
+                out[((int64_t)cu[s] + q) * Cd + c] = silu(v);
+            }
+            for (int i = 0; i < Wc; ++i) st[i] = stream[L + i];
+        }
+    }
+    free(stream);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* prefill (i): the step recurrence, token by token                                      */
 /* ------------------------------------------------------------------------------------ */
 

@@ -262,6 +262,78 @@ def test_conv_matches_numpy_convolve(Wc, ntok):
 
 
 # ----------------------------------------------------------------------------------------
+# varlen prefill conv
+# ----------------------------------------------------------------------------------------
+
+def _lfilter_stream(stream, taps):
+    """Causal FIR by scipy.signal.lfilter: out[m] = sum_k taps[k] * stream[m - (W-1) + k]."""
+    from scipy.signal import lfilter
+    return lfilter(taps[::-1], [1.0], stream)
+
+
+@pytest.mark.parametrize("with_init", [False, True])
+def test_conv_varlen_matches_lfilter(with_init):
+    """Each sequence is an FIR filter over [its stored window (or zeros), its inputs]; lengths
+    cover empty, shorter than the window, exactly the window, and long sequences."""
+    g = _rng(40 + with_init)
+    Cd, W, Wc = 6, 4, 5
+    lengths = [0, 1, 2, 5, 9, 0, 23]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    u = g.standard_normal((int(cu[-1]), Cd))
+    w = g.standard_normal((Cd, W))
+    b = g.standard_normal(Cd)
+    st = g.standard_normal((len(lengths), Cd, Wc))
+    init = np.array([with_init] * len(lengths), np.uint8)
+    st2, out = oracle.conv_varlen(cu, u, w, b, state=st, init=init)
+    for s, L in enumerate(lengths):
+        for c in range(Cd):
+            head = st[s, c] if with_init else np.zeros(Wc)
+            stream = np.concatenate([head, u[cu[s]:cu[s + 1], c]])
+            v = _lfilter_stream(stream, w[c])[Wc:] + b[c]
+            np.testing.assert_allclose(out[cu[s]:cu[s + 1], c], v * expit(v), rtol=1e-13, atol=1e-14)
+            np.testing.assert_array_equal(st2[s, c], stream[-Wc:])
+    assert not np.isnan(out).any()
+
+
+def test_conv_varlen_continues_like_decode_steps():
+    """A prompt split into two prefill calls (the second starting from the window the first
+    wrote) equals one call, and both equal decoding the prompt one token at a time."""
+    g = _rng(42)
+    Cd, W, Wc, L = 5, 4, 3, 17
+    u = g.standard_normal((L, Cd))
+    w = g.standard_normal((Cd, W))
+    st0 = g.standard_normal((1, Cd, Wc))
+    one = np.array([1], np.uint8)
+    st_all, out_all = oracle.conv_varlen([0, L], u, w, state=st0, init=one)
+    st_a, out_a = oracle.conv_varlen([0, 6], u[:6], w, state=st0, init=one)
+    st_b, out_b = oracle.conv_varlen([0, L - 6], u[6:], w, state=st_a, init=one)
+    np.testing.assert_allclose(np.concatenate([out_a, out_b]), out_all, rtol=1e-15)
+    np.testing.assert_array_equal(st_b, st_all)
+    s = st0[0].copy()
+    for t in range(L):
+        s, o = oracle.conv_update(s, u[t:t + 1], w)
+        np.testing.assert_allclose(o[0], out_all[t], rtol=1e-15)
+    np.testing.assert_array_equal(s, st_all[0])
+
+
+def test_conv_varlen_without_init_ignores_stored_window():
+    """A sequence that does not start from its state sees zeros before its first input: its
+    first output is SiLU(w[c, W-1] u_0 + b), and the stored window plays no part."""
+    g = _rng(43)
+    Cd, W, Wc = 4, 4, 3
+    u = g.standard_normal((2, Cd))
+    w = g.standard_normal((Cd, W))
+    b = g.standard_normal(Cd)
+    st = g.standard_normal((1, Cd, Wc))
+    st2, out = oracle.conv_varlen([0, 2], u, w, b, state=st, init=np.array([0], np.uint8))
+    v0 = w[:, W - 1] * u[0] + b
+    v1 = w[:, W - 2] * u[0] + w[:, W - 1] * u[1] + b
+    np.testing.assert_allclose(out[0], v0 * expit(v0), rtol=1e-14)
+    np.testing.assert_allclose(out[1], v1 * expit(v1), rtol=1e-14)
+    np.testing.assert_array_equal(st2[0], np.stack([np.zeros(Cd), u[0], u[1]], axis=1))
+
+
+# ----------------------------------------------------------------------------------------
 # the SSD identity and the chunk decomposition
 # ----------------------------------------------------------------------------------------
 
