@@ -51,6 +51,13 @@ def prefill_bytes(T: int, nseq: int, n_state_writes: int) -> int:
     return T * H * P * 2 + 2 * T * G * N * 2 + T * H * 4 + T * H * P * 2 + n_state_writes * H * P * N * 2
 
 
+def prefill_conv_bytes(T: int, nseq: int) -> int:
+    """Algorithmic bytes of the varlen prefill conv: xBC in, x | B | C out, each sequence's conv
+    window read (W-1 columns) and written (W-1 columns), bf16."""
+    Cd = SHAPE.conv_dim
+    return 2 * T * Cd * 2 + nseq * Cd * (SHAPE.conv_kernel - 1) * 2 * 2
+
+
 def prefill_flops(lengths, chunk: int) -> float:
     """Algorithmic flops of the chunked form (causal halves of the intra-chunk matmuls counted):
     per chunk of length L and group: C B^T L(L+1)/2 * 2N; per head: masked (G . L) X L(L+1)/2 * 2P,
@@ -259,6 +266,22 @@ class PrefillWorkload:
         self.ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         self.interval = interval
         self.n_state_writes = nseq + n_ckpt
+        # raw xBC and conv windows for the conv in front of the scan (every sequence continues
+        # from its stored window)
+        self.xbc = torch.from_numpy(wl.prefill_xbc(g, SHAPE, T, wl.BF16).view(np.int16)).to(dev).view(bf)
+        self.conv_pool = torch.from_numpy(
+            wl.initial_states(g, SHAPE, nseq, wl.F32, wl.BF16)["conv"].view(np.int16)).to(dev).view(bf)
+        self.has_init = torch.ones(nseq, dtype=torch.uint8, device=dev)
+
+    def step_conv(self):
+        T = self.T
+        self.bd.mamba_conv_varlen(self.desc, self.cu, self.xbc, self.prm["conv_w"], self.x.view(T, H * P),
+                                  self.B.view(T, G * N), self.C.view(T, G * N), conv_pool=self.conv_pool,
+                                  slot_ids=self.slot, has_initial_state=self.has_init)
+
+    def step_layer(self):
+        self.step_conv()
+        self.step()
 
     def step(self):
         self.bd.mamba_chunk_scan(self.desc, self.pool, self.cu, self.slot, self.x, self.dt, self.prm["A"], self.B,
@@ -508,6 +531,15 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
         "launches_per_layer": 2,
         "kernel": "k_ssd_tc (tcgen05) after k_tc_meta",
     }
+    ms_conv = _max_over_ranks(torch, dist, _time(torch, pre.step_conv, args.steps, max(args.warmup, 3), dist))
+    by_conv = prefill_conv_bytes(pre.T, len(pre.lengths))
+    prefill["conv"] = {
+        "ms_per_layer": ms_conv, "gbs": by_conv / (ms_conv * 1e-3) / 1e9,
+        "hbm_frac": by_conv / (ms_conv * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by_conv,
+        "launches_per_layer": 2, "kernel": "k_conv_varlen, then k_conv_varlen_state",
+    }
+    ms_layer = _max_over_ranks(torch, dist, _time(torch, pre.step_layer, args.steps, max(args.warmup, 3), dist))
+    prefill["conv_then_scan"] = {"ms_per_layer": ms_layer, "tokens_per_s": pre.T * world / (ms_layer * 1e-3)}
     del pre
     torch.cuda.empty_cache()
     return prefill

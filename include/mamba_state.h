@@ -189,6 +189,45 @@ int mamba_spec_commit(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_
 /* ---------------------------------------------------------------------------------------- */
 
 /*
+ * mamba_conv_varlen -- the causal depthwise conv1d + SiLU that produces the scan's x, B and C
+ * for a varlen prefill batch, continuing each sequence from its stored conv state and leaving
+ * the conv state a later chunk or decode step continues from [P4 x = SiLU(Conv1d(x')); P1 the
+ * conv state object, a window of the most recent inputs, carried across prefill chunks like the
+ * temporal state (has_initial_states)].  For sequence s (tokens [cu_seqlens[s],
+ * cu_seqlens[s+1]), length L) define its input stream
+ *     e(q) = xbc[cu_seqlens[s] + q, c]                    for 0 <= q < L,
+ *     e(q) = conv state column Wc + q of slot_ids[s]      for -Wc <= q < 0 when
+ *            has_initial_state[s] != 0, else 0,
+ * then  out[cu_seqlens[s] + q, c] = SiLU(conv_b[c] + sum_{k<W} conv_w[c, k] * e(q - (W-1) + k))
+ * is split by channel into x_out (c < nheads*head_dim), B_out and C_out (the two blocks of
+ * n_groups*d_state channels that follow), and afterwards the slot's conv state column i holds
+ * e(L - Wc + i), i = 0..Wc-1 (Wc = conv_kernel-1+num_spec): the last Wc inputs of the stream.
+ *
+ *   conv_pool        as in mamba_conv_update, or NULL: then every sequence starts from zeros,
+ *                    no conv state is read or written, and slot_ids / has_initial_state are
+ *                    ignored.
+ *   cu_seqlens       (nseq + 1) int32 as in mamba_chunk_scan (bad values: MAMBA_ERR_SEQLENS,
+ *                    nothing written).
+ *   slot_ids         (nseq) int32; -1: outputs computed from zeros, no state written; outside
+ *                    [-1, num_slots): MAMBA_ERR_SLOT_RANGE and that sequence's outputs and
+ *                    state are left untouched.
+ *   has_initial_state (nseq) uint8 or NULL (all zero).
+ *   xbc              (total_tokens, conv_dim) act_dtype raw inputs, 16-byte aligned.
+ *   conv_w (conv_dim, conv_kernel) fp32;  conv_b (conv_dim) fp32 or NULL.
+ *   x_out            (total_tokens, nheads*head_dim) act_dtype, 16-byte aligned.
+ *   B_out, C_out     (total_tokens, n_groups*d_state) act_dtype, 16-byte aligned.
+ * Requires nheads*head_dim and n_groups*d_state to be multiples of 16 bytes' worth of act_dtype
+ * elements (MAMBA_EUNSUPPORTED otherwise).  Two kernels run in stream order: the conv, then the
+ * state write-back.
+ */
+int mamba_conv_varlen(const mamba_layer_desc *desc, void *conv_pool, int64_t conv_slot_stride,
+                      int64_t num_slots, const int32_t *cu_seqlens, int32_t nseq,
+                      int32_t total_tokens, const int32_t *slot_ids,
+                      const uint8_t *has_initial_state, const void *xbc, const float *conv_w,
+                      const float *conv_b, void *x_out, void *B_out, void *C_out,
+                      int32_t *err_word, void *stream);
+
+/*
  * Bytes of device workspace mamba_chunk_scan needs for these sizes (0 on a bad argument).
  */
 size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *desc, int32_t total_tokens,

@@ -61,6 +61,8 @@ SIGNATURES = {
     "mamba_state_update": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
                                           _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mamba_spec_commit": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
+    "mamba_conv_varlen": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _vp]),
     "mamba_chunk_scan_workspace_bytes": (_sz, [_dp, _i32, _i32, _i32]),
     "mamba_chunk_scan": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -182,6 +184,21 @@ def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept
 # ------------------------------------------------------------------------------------------
 # prefill
 # ------------------------------------------------------------------------------------------
+
+def mamba_conv_varlen(desc: LayerDesc, cu_seqlens, xbc, conv_w, x_out, B_out, C_out, *, conv_pool=None,
+                      slot_ids=None, has_initial_state=None, conv_b=None, err_word=None, stream=None):
+    """Varlen causal conv1d + SiLU of a prefill batch into x | B | C, continuing each sequence
+    from its conv state and writing the state back (when ``conv_pool`` is given)."""
+    nseq = int(cu_seqlens.shape[0]) - 1
+    total = int(xbc.shape[0])
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    num_slots = conv_pool.shape[0] if conv_pool is not None else 0
+    rc = lib().mamba_conv_varlen(ctypes.byref(desc), _ptr(conv_pool), conv_stride, num_slots, _cptr(cu_seqlens),
+                                 nseq, total, _cptr(slot_ids), _cptr(has_initial_state), _cptr(xbc), _cptr(conv_w),
+                                 _cptr(conv_b), _cptr(x_out), _cptr(B_out), _cptr(C_out), _ptr(err_word),
+                                 _stream(stream))
+    _check(rc, "mamba_conv_varlen")
+
 
 def mamba_chunk_scan(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x, dt, A, B, C, y, workspace, *,
                      has_initial_state=None, ckpt_slots=None, ckpt_interval=0, chunk=256, D=None, dt_bias=None,

@@ -214,6 +214,11 @@ def prefill_inputs(g: np.random.Generator, shape: LayerShape, params: dict, T: i
     return dict(x=x, B=B, C=C, dt=dt, z=z)
 
 
+def prefill_xbc(g: np.random.Generator, shape: LayerShape, T: int, act: str) -> np.ndarray:
+    """Raw (pre-conv) prefill rows xBC (T, conv_dim), distributed like the decode inputs."""
+    return store(xbc_values(g, shape, (T,)), act)
+
+
 def accept_lengths(g: np.random.Generator, batch: int, ntok: int) -> np.ndarray:
     """Accepted draft counts, uniform in 0..ntok."""
     return g.integers(0, ntok + 1, size=batch).astype(np.int32)

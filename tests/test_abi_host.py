@@ -184,3 +184,27 @@ def test_chunk_scan_host_errors(lib):
     assert call(chunk=100) == bd.MAMBA_EUNSUPPORTED  # neither a tensor-core nor a portable chunk
     assert call(ck=FAKE, mc=4, ci=1000) == bd.MAMBA_EINVAL  # interval not a multiple of the chunk
     assert call(ws=FAKE + 4) == bd.MAMBA_EALIGN
+
+
+def test_conv_varlen_host_errors(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+
+    def call(**over):
+        a = dict(pool=FAKE, stride=10240 * 3, ns=8, cu=FAKE, nseq=2, T=100, slot=FAKE, xbc=FAKE, w=FAKE,
+                 x=FAKE, B=FAKE, C=FAKE, dd=d)
+        a.update(over)
+        return lib.mamba_conv_varlen(ctypes.byref(a["dd"]), a["pool"], a["stride"], a["ns"], a["cu"], a["nseq"],
+                                     a["T"], a["slot"], None, a["xbc"], a["w"], None, a["x"], a["B"], a["C"],
+                                     None, None)
+
+    assert call(nseq=0, T=0) == bd.MAMBA_OK
+    assert call(nseq=0, T=5) == bd.MAMBA_EINVAL
+    assert call(cu=None) == bd.MAMBA_EINVAL
+    assert call(w=None) == bd.MAMBA_EINVAL
+    assert call(B=None) == bd.MAMBA_EINVAL
+    assert call(slot=None) == bd.MAMBA_EINVAL  # a conv pool needs slot ids
+    assert call(stride=10) == bd.MAMBA_EINVAL
+    assert call(x=FAKE + 2) == bd.MAMBA_EALIGN
+    assert call(xbc=FAKE + 8) == bd.MAMBA_EALIGN
+    odd = bd.layer_desc(wl.LayerShape(nheads=3, head_dim=2, d_state=8, n_groups=1, conv_kernel=4))
+    assert call(dd=odd, stride=(6 + 16) * 3) == bd.MAMBA_EUNSUPPORTED  # x block of 6 bf16 is not 16 bytes
