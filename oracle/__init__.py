@@ -63,6 +63,12 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_spec_commit.argtypes = [i64, i32, i32, i32, i32, _dp, i64, _dp, i64, _ip, _ip, _ip]
         lib.oracle_spec_commit.restype = i32
+        _i8 = ctypes.POINTER(ctypes.c_int8)
+        _fp = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_int8_quantize.argtypes = [i32, i32, i32, _dp, _i8, _fp]
+        lib.oracle_int8_quantize.restype = None
+        lib.oracle_int8_dequantize.argtypes = [i32, i32, i32, _i8, _fp, _dp]
+        lib.oracle_int8_dequantize.restype = None
         lib.oracle_conv_varlen.argtypes = [i32, i32, i32, i32, _ip, ctypes.POINTER(ctypes.c_uint8), _dp,
                                            _dp, _dp, _dp, _dp]
         lib.oracle_conv_varlen.restype = i32
@@ -205,6 +211,33 @@ def spec_commit(ssm_pool, slot, scratch, accept, *, conv_pool=None):
 # --------------------------------------------------------------------------------------
 # prefill
 # --------------------------------------------------------------------------------------
+
+def int8_quantize(state):
+    """Per-(head, k-channel) symmetric int8 quantisation of a temporal state H x P x N (the
+    k-channel is the d_state index n).  Follows the int8 checkpoint store of "Hybrid SSM / Mamba
+    models and non-KV state" (quantised once on store); computed in float32, the precision the
+    codes are decided in.  Returns (q int8 H x P x N, scale float32 H x N)."""
+    lib = _load()
+    st = _f64(state)
+    H, P, N = st.shape
+    q = np.zeros((H, P, N), np.int8)
+    sc = np.zeros((H, N), np.float32)
+    lib.oracle_int8_quantize(H, P, N, _p(st), q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
+                             sc.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return q, sc
+
+
+def int8_dequantize(q, scale):
+    """state' = q * scale (float32 product), as float64 values (dequantised once on a hit)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    sc = np.ascontiguousarray(scale, dtype=np.float32)
+    H, P, N = q.shape
+    out = np.empty((H, P, N), np.float64)
+    lib.oracle_int8_dequantize(H, P, N, q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
+                               sc.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), _p(out))
+    return out
+
 
 def conv_varlen(cu_seqlens, u, w, b=None, *, state=None, init=None):
     """Varlen causal conv1d + SiLU of a prefill batch, with the conv state carried in and out.

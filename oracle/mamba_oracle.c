@@ -323,6 +323,55 @@ int oracle_spec_commit(int64_t ssm_elems, int Cd, int Wc, int ntok, int batch, d
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* int8 checkpoint store: per-(head, k-channel) symmetric quantisation                   */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * A cached checkpoint of the temporal state kept in int8, one scale per (head, k-channel),
+ * symmetric ("Hybrid SSM / Mamba models and non-KV state", the SGLang checkpoint-store
+ * paragraph: quantised once on store, dequantised once into a fresh active slot on a hit).
+ * The state is H x P x N; its k-channel is the d_state index n (B_t, the key of each update
+ * x_t B_t^T, runs along n), so a scale covers the P values of one (h, n):
+ *     amax = max_p |state[h,p,n]|,   s[h,n] = amax / 127,
+ *     q[h,p,n] = clamp(rint(state[h,p,n] / s[h,n]), -127, 127)   (s == 0: q = 0).
+ * The codes are integers decided by floating point, so this is computed in float32, the
+ * precision the quantiser runs in (rint: round half to even).
+ */
+void oracle_int8_quantize(int H, int P, int N, const double *state, int8_t *q, float *scale) {
+    for (int h = 0; h < H; ++h) {
+        for (int n = 0; n < N; ++n) {
+            float amax = 0.0f;
+            for (int p = 0; p < P; ++p) {
+                const float v = fabsf((float)state[((int64_t)h * P + p) * N + n]);
+                if (v > amax) amax = v;
+            }
+            const float sc = amax / 127.0f;
+            scale[(int64_t)h * N + n] = sc;
+            for (int p = 0; p < P; ++p) {
+                const int64_t i = ((int64_t)h * P + p) * N + n;
+                float r = 0.0f;
+                if (sc > 0.0f) {
+                    r = rintf((float)state[i] / sc);
+                    if (r > 127.0f) r = 127.0f;
+                    if (r < -127.0f) r = -127.0f;
+                }
+                q[i] = (int8_t)r;
+            }
+        }
+    }
+}
+
+/* Dequantise: state'[h,p,n] = q[h,p,n] * s[h,n], the product in float32. */
+void oracle_int8_dequantize(int H, int P, int N, const int8_t *q, const float *scale, double *out) {
+    for (int h = 0; h < H; ++h)
+        for (int p = 0; p < P; ++p)
+            for (int n = 0; n < N; ++n) {
+                const int64_t i = ((int64_t)h * P + p) * N + n;
+                out[i] = (double)((float)q[i] * scale[(int64_t)h * N + n]);
+            }
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* prefill: varlen causal conv1d + SiLU, conv state read at the start and written back   */
 /* ------------------------------------------------------------------------------------ */
 

@@ -262,6 +262,92 @@ def test_conv_matches_numpy_convolve(Wc, ntok):
 
 
 # ----------------------------------------------------------------------------------------
+# int8 checkpoint store
+# ----------------------------------------------------------------------------------------
+
+def _int8_state(seed, H=3, P=16, N=8):
+    """States whose (head, k-channel) columns span many magnitudes, with one all-zero column."""
+    g = _rng(seed)
+    st = g.standard_normal((H, P, N)) * np.exp(g.uniform(-8, 8, size=(H, 1, N)))
+    st[1, :, 3] = 0.0
+    return st
+
+
+def test_int8_codes_range_and_column_max():
+    st = _int8_state(50)
+    q, sc = oracle.int8_quantize(st)
+    assert q.dtype == np.int8 and sc.dtype == np.float32 and sc.shape == (3, 8)
+    assert np.abs(q.astype(np.int32)).max() <= 127
+    for h in range(3):
+        for n in range(8):
+            col = st[h, :, n]
+            if not col.any():
+                assert sc[h, n] == 0 and not q[h, :, n].any()
+                continue
+            assert np.abs(q[h, :, n].astype(np.int32)).max() == 127  # the column's extreme maps to 127
+            assert np.sign(q[h, :, n][np.abs(q[h, :, n]) == 127][0]) == np.sign(col[np.argmax(np.abs(col))])
+            np.testing.assert_allclose(sc[h, n], np.abs(col).max() / 127, rtol=1e-6)
+
+
+def test_int8_roundtrip_error_is_half_a_step():
+    st = _int8_state(51)
+    q, sc = oracle.int8_quantize(st)
+    back = oracle.int8_dequantize(q, sc)
+    err = np.abs(back - st)
+    bound = 0.5 * sc[:, None, :].astype(np.float64) * (1 + 1e-5) + 1e-30
+    assert (err <= bound).all()
+    # dequantisation is the product of the code and its column's scale
+    np.testing.assert_array_equal(back, (q.astype(np.float32) * sc[:, None, :]).astype(np.float64))
+
+
+def test_int8_scale_belongs_to_one_head_and_k_channel():
+    """Growing one element changes only its own (head, k-channel) scale and codes."""
+    st = _int8_state(52)
+    q, sc = oracle.int8_quantize(st)
+    st2 = st.copy()
+    st2[2, 5, 6] = 10 * np.abs(st[2, :, 6]).max()
+    q2, sc2 = oracle.int8_quantize(st2)
+    mask = np.ones_like(sc, bool)
+    mask[2, 6] = False
+    np.testing.assert_array_equal(sc2[mask], sc[mask])
+    assert sc2[2, 6] > sc[2, 6]
+    qmask = np.ones_like(q, bool)
+    qmask[2, :, 6] = False
+    np.testing.assert_array_equal(q2[qmask], q[qmask])
+
+
+def test_int8_power_of_two_scaling_keeps_codes():
+    st = _int8_state(53)
+    q, sc = oracle.int8_quantize(st)
+    q2, sc2 = oracle.int8_quantize(st * 32.0)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(sc2, sc * np.float32(32.0))
+
+
+def test_restored_int8_state_error_follows_the_recurrence():
+    """With the same inputs after a restore, the state error evolves as the product of the decays
+    (the page's Delta S_{t+m} = (A_{t+m} ... A_{t+1}) Delta S_t), and the output error is its
+    image under C."""
+    H, P, N, G, T = 4, 3, 5, 2, 24
+    pr = _random_problem(54, H=H, P=P, N=N, G=G, T=T)
+    h = 0.1 * _rng(55).standard_normal((H, P, N))
+    q, sc = oracle.int8_quantize(h)
+    h_r = oracle.int8_dequantize(q, sc)
+    hA, yA, hsA = oracle.ssm_update(h, pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"], D=pr["D"],
+                                    dt_bias=pr["dt_bias"], record=True)
+    hB, yB, hsB = oracle.ssm_update(h_r, pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"], D=pr["D"],
+                                    dt_bias=pr["dt_bias"], record=True)
+    delta = np.log1p(np.exp(pr["dt"] + pr["dt_bias"][None, :]))  # T x H
+    decay = np.cumprod(np.exp(delta * pr["A"][None, :]), axis=0)  # T x H
+    d0 = h - h_r
+    for t in range(T):
+        expect = decay[t][:, None, None] * d0
+        np.testing.assert_allclose(hsA[t] - hsB[t], expect, rtol=1e-9, atol=1e-15)
+        C_t = np.stack([pr["C"][t, _group(hh, H, G)] for hh in range(H)])  # H x N
+        np.testing.assert_allclose(yA[t] - yB[t], np.einsum("hpn,hn->hp", expect, C_t), rtol=1e-8, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------------------
 # varlen prefill conv
 # ----------------------------------------------------------------------------------------
 
