@@ -366,11 +366,13 @@ def run_gpu(args):
     bld.build()
     hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
 
-    if args.only in ("prefill", "spec", "sweep"):
+    if args.only in ("prefill", "spec", "sweep", "checkpoint"):
         if args.only == "prefill":
             res = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
         elif args.only == "spec":
             res = run_spec(torch, args, rank, dist, hbm_peak)
+        elif args.only == "checkpoint":
+            res = run_checkpoint(torch, args, rank, dist, hbm_peak)
         else:
             res = run_sweep(torch, args, rank, dist, hbm_peak)
         if rank == 0:
@@ -404,13 +406,15 @@ def run_gpu(args):
                "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
     del dec
     torch.cuda.empty_cache()
-    prefill = spec = sweep = None
+    prefill = spec = sweep = ckpt = None
     if args.only == "all":
         prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
         torch.cuda.empty_cache()
         spec = run_spec(torch, args, rank, dist, hbm_peak)
         torch.cuda.empty_cache()
         sweep = run_sweep(torch, args, rank, dist, hbm_peak)
+        torch.cuda.empty_cache()
+        ckpt = run_checkpoint(torch, args, rank, dist, hbm_peak)
         torch.cuda.empty_cache()
 
     cpu = None
@@ -419,7 +423,7 @@ def run_gpu(args):
 
     if rank == 0:
         emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck,
-             prefill, cpu, spec, sweep)
+             prefill, cpu, spec, sweep, ckpt)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -517,6 +521,46 @@ def run_sweep(torch, args, rank, dist, hbm_peak):
     return {"workload": SWEEP["name"], "points": out}
 
 
+CKPT_ROWS = 256  # slots restored, stored or loaded per call
+
+
+def run_checkpoint(torch, args, rank, dist, hbm_peak):
+    """Prefix-cache checkpoint operations at the Nemotron-H-8B shape on a 512-slot bf16 pool:
+    restore (copy) of 256 slots into fresh slots, int8 store of 256 slots, int8 load of 256
+    entries.  GB/s = algorithmic bytes (each state read once and written once) / time."""
+    from recurrent_state_update_gb300 import binding as bd
+    dev = torch.device("cuda")
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7000 + rank)
+    S = DECODE["pool"]
+    ssm = torch.randn(S, H, P, N, generator=gen, device=dev).mul_(0.1).to(bf)
+    conv = torch.randn(S, CD, W1, generator=gen, device=dev).mul_(0.1).to(bf)
+    desc = bd.layer_desc(SHAPE)
+    eb = bd.mamba_int8_entry_bytes(desc)
+    store = torch.empty(CKPT_ROWS * eb, dtype=torch.uint8, device=dev)
+    g = wl.rng(7000 + rank, 0)
+    perm = g.permutation(S).astype(np.int32)
+    src = torch.from_numpy(perm[:CKPT_ROWS].copy()).to(dev)
+    dst = torch.from_numpy(perm[CKPT_ROWS:2 * CKPT_ROWS].copy()).to(dev)
+    ent = torch.from_numpy(g.permutation(CKPT_ROWS).astype(np.int32)).to(dev)
+    st_b, cv_b = H * P * N * 2, CD * W1 * 2
+    q_b = H * P * N + H * N * 4 + cv_b
+    legs = {
+        "restore_copy": (lambda: bd.mamba_slot_copy(desc, ssm, src, dst, conv_pool=conv), 2 * (st_b + cv_b)),
+        "int8_store": (lambda: bd.mamba_ckpt_store_int8(desc, ssm, src, ent, store, conv_pool=conv), st_b + cv_b + q_b),
+        "int8_load": (lambda: bd.mamba_ckpt_load_int8(desc, ssm, ent, dst, store, conv_pool=conv), q_b + st_b + cv_b),
+    }
+    out = {"workload": f"{CKPT_ROWS} slots of a {S}-slot Nemotron-H-8B bf16 pool (2 MiB SSM + 60 KiB conv each)",
+           "int8_entry_bytes": eb}
+    for name, (fn, per_row) in legs.items():
+        ms = _max_over_ranks(torch, dist, _time(torch, fn, max(args.steps, 20), max(args.warmup, 3), dist))
+        gbs = CKPT_ROWS * per_row / (ms * 1e-3) / 1e9
+        out[name] = {"us_per_call": ms * 1e3, "gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                     "algorithmic_bytes": CKPT_ROWS * per_row}
+    return out
+
+
 def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
     pre = PrefillWorkload(torch, rank)
     ms_pre = _max_over_ranks(torch, dist, _time(torch, pre.step, args.steps, max(args.warmup, 3), dist))
@@ -546,7 +590,7 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
 
 
 def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
-         cpu, spec=None, sweep=None):
+         cpu, spec=None, sweep=None, ckpt=None):
     line = {
         "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -568,6 +612,7 @@ def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_
         "prefill": prefill,
         "spec_decode": spec,
         "padding_sweep": sweep,
+        "checkpoint": ckpt,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -632,7 +677,7 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--layers", type=int, default=0, help="decode layers per step (default: the workload's 48)")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "spec", "sweep"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "spec", "sweep", "checkpoint"], default="all",
                     help="time one form alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps

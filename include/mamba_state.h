@@ -273,6 +273,71 @@ int mamba_chunk_scan(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_s
                      void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream);
 
 /* ---------------------------------------------------------------------------------------- */
+/* prefix-cache checkpoints: slot copy and the int8 checkpoint store                        */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * mamba_slot_copy -- batched slot-to-slot copy of whole states [P1: on a prefix-cache hit the
+ * cached state is copied into a fresh slot rather than shared (copy-on-write), since the
+ * recurrence updates its slot in place].  For each i with src_slots[i] and dst_slots[i] both
+ * != -1, the SSM state (and, when conv_pool is given, the conv state) of slot src_slots[i] is
+ * copied bit for bit into slot dst_slots[i]; src == dst is a no-op.
+ *   ssm_pool, conv_pool, strides, num_slots   as in mamba_state_update / mamba_conv_update.
+ *   src_slots, dst_slots  (n) int32; an id outside [-1, num_slots): MAMBA_ERR_SLOT_RANGE and
+ *                         that row is skipped.  dst ids must be distinct and no dst may be
+ *                         another row's src.
+ * Alignment: pools, slot strides and the per-slot state sizes in bytes multiples of 16.
+ * Limits: n <= 65535.
+ */
+int mamba_slot_copy(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                    int64_t num_slots, void *conv_pool, int64_t conv_slot_stride,
+                    const int32_t *src_slots, const int32_t *dst_slots, int32_t n,
+                    int32_t *err_word, void *stream);
+
+/*
+ * Bytes of one entry of the int8 checkpoint store (0 on a bad desc).  An entry holds, each
+ * section starting on a 256-byte boundary: the codes q (nheads, head_dim, d_state) int8; the
+ * scales (nheads, d_state) fp32; the conv window (conv_dim, conv_kernel-1+num_spec) in
+ * conv_dtype.  At the Nemotron-H-8B shape an entry is about 1.1 MB against 2 MiB for a bf16 slot.
+ */
+size_t mamba_int8_entry_bytes(const mamba_layer_desc *desc);
+
+/*
+ * mamba_ckpt_store_int8 -- quantise cached states into the int8 store [P1: SGLang's checkpoint
+ * store keeps cached temporal states in int8, symmetric per (head, k-channel), quantised once on
+ * store; the conv window is kept at its native dtype].  The k-channel of the temporal state
+ * (nheads, head_dim, d_state) is the d_state index n, so for each head h and n of slot
+ * src_slots[i], in fp32:
+ *     a = max_p |state[h, p, n]|,   s[h, n] = a / 127,
+ *     q[h, p, n] = clamp(rint(state[h, p, n] * (127 / a)), -127, 127)   (0 where a == 0),
+ * written to entry dst_entries[i] of `store` together with a copy of the slot's conv window
+ * (when conv_pool is given).
+ *   store        device buffer of num_entries * mamba_int8_entry_bytes(desc) bytes, 16-byte
+ *                aligned; entry e starts at e * mamba_int8_entry_bytes(desc).
+ *   src_slots, dst_entries  (n) int32, -1 = skip the row; out of range: MAMBA_ERR_SLOT_RANGE.
+ * Requires d_state a multiple of 8, d_state <= 512 and 4 * head_dim * d_state state elements to
+ * fit in 200 KB (MAMBA_EUNSUPPORTED otherwise); alignment as in
+ * mamba_slot_copy.
+ */
+int mamba_ckpt_store_int8(const mamba_layer_desc *desc, const void *ssm_pool, int64_t ssm_slot_stride,
+                          const void *conv_pool, int64_t conv_slot_stride, int64_t num_slots,
+                          const int32_t *src_slots, const int32_t *dst_entries, int32_t n,
+                          void *store, int64_t num_entries, int32_t *err_word, void *stream);
+
+/*
+ * mamba_ckpt_load_int8 -- dequantise entries into fresh active slots [P1: dequantised once into
+ * a fresh active slot on a hit]: state[h, p, n] = q[h, p, n] * s[h, n] (fp32 product, stored in
+ * state_dtype, bf16 round to nearest even), and the entry's conv window copied into the slot's
+ * conv state (when conv_pool is given).
+ *   src_entries, dst_slots  (n) int32, -1 = skip; out of range: MAMBA_ERR_SLOT_RANGE.
+ * Other arguments and limits as in mamba_ckpt_store_int8.
+ */
+int mamba_ckpt_load_int8(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                         void *conv_pool, int64_t conv_slot_stride, int64_t num_slots,
+                         const int32_t *src_entries, const int32_t *dst_slots, int32_t n,
+                         const void *store, int64_t num_entries, int32_t *err_word, void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
 /* chunked prefill without a caller workspace                                               */
 /* ---------------------------------------------------------------------------------------- */
 

@@ -332,8 +332,9 @@ int oracle_spec_commit(int64_t ssm_elems, int Cd, int Wc, int ntok, int batch, d
  * paragraph: quantised once on store, dequantised once into a fresh active slot on a hit).
  * The state is H x P x N; its k-channel is the d_state index n (B_t, the key of each update
  * x_t B_t^T, runs along n), so a scale covers the P values of one (h, n):
- *     amax = max_p |state[h,p,n]|,   s[h,n] = amax / 127,
- *     q[h,p,n] = clamp(rint(state[h,p,n] / s[h,n]), -127, 127)   (s == 0: q = 0).
+ *     amax = max_p |state[h,p,n]|,   s[h,n] = amax / 127,   r[h,n] = 127 / amax,
+ *     q[h,p,n] = clamp(rint(state[h,p,n] * r[h,n]), -127, 127)   (amax == 0: s = 0, q = 0):
+ * the nearest code on the grid of step s, reached by multiplying with the reciprocal step.
  * The codes are integers decided by floating point, so this is computed in float32, the
  * precision the quantiser runs in (rint: round half to even).
  */
@@ -346,12 +347,13 @@ void oracle_int8_quantize(int H, int P, int N, const double *state, int8_t *q, f
                 if (v > amax) amax = v;
             }
             const float sc = amax / 127.0f;
+            const float rs = amax > 0.0f ? 127.0f / amax : 0.0f;
             scale[(int64_t)h * N + n] = sc;
             for (int p = 0; p < P; ++p) {
                 const int64_t i = ((int64_t)h * P + p) * N + n;
                 float r = 0.0f;
-                if (sc > 0.0f) {
-                    r = rintf((float)state[i] / sc);
+                if (amax > 0.0f) {
+                    r = rintf((float)state[i] * rs);
                     if (r > 127.0f) r = 127.0f;
                     if (r < -127.0f) r = -127.0f;
                 }

@@ -63,6 +63,10 @@ SIGNATURES = {
     "mamba_spec_commit": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
     "mamba_conv_varlen": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
+    "mamba_slot_copy": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _i32, _vp, _vp]),
+    "mamba_int8_entry_bytes": (_sz, [_dp]),
+    "mamba_ckpt_store_int8": (ctypes.c_int, [_dp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i64, _vp, _vp]),
+    "mamba_ckpt_load_int8": (ctypes.c_int, [_dp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i64, _vp, _vp]),
     "mamba_chunk_scan_workspace_bytes": (_sz, [_dp, _i32, _i32, _i32]),
     "mamba_chunk_scan": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -179,6 +183,50 @@ def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept
                                  _ptr(conv_pool), conv_stride, _cptr(slot_ids), _cptr(scratch_slots),
                                  _cptr(accept_len), batch, ntok, _ptr(err_word), _stream(stream))
     _check(rc, "mamba_spec_commit")
+
+
+# ------------------------------------------------------------------------------------------
+# prefix-cache checkpoints
+# ------------------------------------------------------------------------------------------
+
+def mamba_slot_copy(desc: LayerDesc, ssm_pool, src_slots, dst_slots, *, conv_pool=None, err_word=None, stream=None):
+    """Copy whole slot states src_slots[i] -> dst_slots[i] (checkpoint restore, copy-on-write)."""
+    n = int(src_slots.shape[0])
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    rc = lib().mamba_slot_copy(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                               _ptr(conv_pool), conv_stride, _cptr(src_slots), _cptr(dst_slots), n, _ptr(err_word),
+                               _stream(stream))
+    _check(rc, "mamba_slot_copy")
+
+
+def mamba_int8_entry_bytes(desc: LayerDesc) -> int:
+    return lib().mamba_int8_entry_bytes(ctypes.byref(desc))
+
+
+def mamba_ckpt_store_int8(desc: LayerDesc, ssm_pool, src_slots, dst_entries, store, *, conv_pool=None,
+                          err_word=None, stream=None):
+    """Quantise slots into int8 store entries (per-(head, d_state channel) symmetric scales)."""
+    n = int(src_slots.shape[0])
+    eb = mamba_int8_entry_bytes(desc)
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    rc = lib().mamba_ckpt_store_int8(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), _ptr(conv_pool),
+                                     conv_stride, ssm_pool.shape[0], _cptr(src_slots), _cptr(dst_entries), n,
+                                     _ptr(store), (store.numel() * store.element_size()) // eb, _ptr(err_word),
+                                     _stream(stream))
+    _check(rc, "mamba_ckpt_store_int8")
+
+
+def mamba_ckpt_load_int8(desc: LayerDesc, ssm_pool, src_entries, dst_slots, store, *, conv_pool=None,
+                         err_word=None, stream=None):
+    """Dequantise int8 store entries into slots."""
+    n = int(src_entries.shape[0])
+    eb = mamba_int8_entry_bytes(desc)
+    conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
+    rc = lib().mamba_ckpt_load_int8(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), _ptr(conv_pool),
+                                    conv_stride, ssm_pool.shape[0], _cptr(src_entries), _cptr(dst_slots), n,
+                                    _ptr(store), (store.numel() * store.element_size()) // eb, _ptr(err_word),
+                                    _stream(stream))
+    _check(rc, "mamba_ckpt_load_int8")
 
 
 # ------------------------------------------------------------------------------------------

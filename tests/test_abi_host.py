@@ -208,3 +208,26 @@ def test_conv_varlen_host_errors(lib):
     assert call(xbc=FAKE + 8) == bd.MAMBA_EALIGN
     odd = bd.layer_desc(wl.LayerShape(nheads=3, head_dim=2, d_state=8, n_groups=1, conv_kernel=4))
     assert call(dd=odd, stride=(6 + 16) * 3) == bd.MAMBA_EUNSUPPORTED  # x block of 6 bf16 is not 16 bytes
+
+
+def test_checkpoint_ops_host_errors(lib):
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    st = 128 * 64 * 128
+    r = lib.mamba_slot_copy(ctypes.byref(d), None, st, 8, None, 0, FAKE, FAKE, 4, None, None)
+    assert r == bd.MAMBA_EINVAL
+    r = lib.mamba_slot_copy(ctypes.byref(d), FAKE, st, 8, None, 0, FAKE, FAKE, 0, None, None)
+    assert r == bd.MAMBA_OK  # nothing to copy
+    r = lib.mamba_slot_copy(ctypes.byref(d), FAKE + 8, st, 8, None, 0, FAKE, FAKE, 4, None, None)
+    assert r == bd.MAMBA_EALIGN
+    r = lib.mamba_slot_copy(ctypes.byref(d), FAKE, st - 1, 8, None, 0, FAKE, FAKE, 4, None, None)
+    assert r == bd.MAMBA_EINVAL
+    eb = lib.mamba_int8_entry_bytes(ctypes.byref(d))
+    # codes (1 MiB) + scales (64 KiB) + conv window (60 KiB), each on a 256-byte boundary
+    assert eb == 128 * 64 * 128 + 128 * 128 * 4 + 10240 * 3 * 2
+    for fn in (lib.mamba_ckpt_store_int8, lib.mamba_ckpt_load_int8):
+        assert fn(ctypes.byref(d), FAKE, st, None, 0, 8, FAKE, FAKE, 4, None, 4, None, None) == bd.MAMBA_EINVAL
+        assert fn(ctypes.byref(d), FAKE, st, None, 0, 8, FAKE, FAKE, 4, FAKE + 4, 4, None, None) == bd.MAMBA_EALIGN
+        assert fn(ctypes.byref(d), FAKE, st, None, 0, 8, FAKE, FAKE, 0, FAKE, 4, None, None) == bd.MAMBA_OK
+    odd = bd.layer_desc(wl.LayerShape(nheads=2, head_dim=4, d_state=12, n_groups=1, conv_kernel=4))
+    assert lib.mamba_ckpt_store_int8(ctypes.byref(odd), FAKE, 96, None, 0, 8, FAKE, FAKE, 4, FAKE, 4, None,
+                                     None) == bd.MAMBA_EUNSUPPORTED
