@@ -63,6 +63,8 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_spec_commit.argtypes = [i64, i32, i32, i32, i32, _dp, i64, _dp, i64, _ip, _ip, _ip]
         lib.oracle_spec_commit.restype = i32
+        lib.oracle_mamba1_update.argtypes = [i32, i32, i32, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, i32, _dp, _dp]
+        lib.oracle_mamba1_update.restype = None
         _i8 = ctypes.POINTER(ctypes.c_int8)
         _fp = ctypes.POINTER(ctypes.c_float)
         lib.oracle_int8_quantize.argtypes = [i32, i32, i32, _dp, _i8, _fp]
@@ -152,6 +154,22 @@ def ssm_update(h, x, B, C, dt, A, D=None, dt_bias=None, dt_softplus=True, z=None
                           _p(_f64(dt)), _p(_f64(A)), _p(_f64(D)), _p(_f64(dt_bias)),
                           int(bool(dt_softplus)), _p(_f64(z)), _p(y))
     return (h, y, h_tok) if record else (h, y)
+
+
+def mamba1_update(h, x, B, C, dt, A, D=None, dt_bias=None, dt_softplus=True, z=None):
+    """Mamba1 (S6) state update of one request over ntok tokens (echobase "Mamba" notes, with a
+    per-channel step and a D x N matrix A; the (D, N) Mamba1 state of "Hybrid SSM / Mamba models
+    and non-KV state").  h: D x N.  x, dt, z: ntok x D.  B, C: ntok x N.  A: D x N.
+    Returns (h_new, y) with y ntok x D."""
+    lib = _load()
+    h = _f64(h).copy()
+    Dn, N = h.shape
+    x = _f64(x)
+    ntok = x.shape[0]
+    y = np.empty((ntok, Dn), np.float64)
+    lib.oracle_mamba1_update(Dn, N, ntok, _p(h), _p(x), _p(_f64(dt)), _p(_f64(A)), _p(_f64(B)), _p(_f64(C)),
+                             _p(_f64(D)), _p(_f64(dt_bias)), int(bool(dt_softplus)), _p(_f64(z)), _p(y))
+    return h, y
 
 
 def decode(ssm_pool, slot, xbc, dt, A, *, conv_pool=None, conv_w=None, conv_b=None, scratch=None,

@@ -185,6 +185,41 @@ void oracle_ssm_update(int H, int P, int N, int G, int ntok, double *h, double *
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Mamba1 (S6): the selective state update with a per-channel step and a (D, N) A        */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * One request of a Mamba1 layer, ntok tokens in order (echobase "Mamba" notes: the Mamba block
+ * equations with B and C input dependent, h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,
+ * y_t = C_t h_t, y_hat = y (.) SiLU(z); the classic output adds D x_t; "Hybrid SSM / Mamba
+ * models and non-KV state": the Mamba1 recurrent state has shape (D, N)).  Here every channel
+ * d of the D = d_inner channels has its own step and its own row of A:
+ *   Delta = softplus(dt[d] + dt_bias[d]) (or dt + dt_bias),
+ *   h[d, n] <- exp(Delta * A[d, n]) * h[d, n] + Delta * B[n] * x[d],
+ *   y[d] = sum_n C[n] * h[d, n] + D[d] * x[d];   y *= SiLU(z[d]) if z.
+ * h: D x N (in/out).  x, dt, z, y: ntok x D.   A: D x N.   Bm, Cm: ntok x N.
+ */
+void oracle_mamba1_update(int D, int N, int ntok, double *h, const double *x, const double *dt,
+                          const double *A, const double *Bm, const double *Cm, const double *Dskip,
+                          const double *dt_bias, int dt_softplus, const double *z, double *y) {
+    for (int j = 0; j < ntok; ++j) {
+        for (int d = 0; d < D; ++d) {
+            const double delta = make_delta(dt[(int64_t)j * D + d], dt_bias, d, dt_softplus);
+            const double xv = x[(int64_t)j * D + d];
+            double *hrow = h + (int64_t)d * N;
+            double acc = 0.0;
+            for (int n = 0; n < N; ++n) {
+                hrow[n] = exp(delta * A[(int64_t)d * N + n]) * hrow[n] + delta * Bm[(int64_t)j * N + n] * xv;
+                acc += Cm[(int64_t)j * N + n] * hrow[n];
+            }
+            double yv = acc + (Dskip ? Dskip[d] * xv : 0.0);
+            if (z) yv *= silu(z[(int64_t)j * D + d]);
+            y[(int64_t)j * D + d] = yv;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* decode over a slot pool                                                               */
 /* ------------------------------------------------------------------------------------ */
 

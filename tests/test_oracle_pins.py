@@ -262,6 +262,60 @@ def test_conv_matches_numpy_convolve(Wc, ntok):
 
 
 # ----------------------------------------------------------------------------------------
+# Mamba1 (S6) state update
+# ----------------------------------------------------------------------------------------
+
+def _mamba1_problem(seed, Dn=6, N=5, T=9):
+    g = _rng(seed)
+    return dict(h=0.3 * g.standard_normal((Dn, N)), x=g.standard_normal((T, Dn)), B=g.standard_normal((T, N)),
+                C=g.standard_normal((T, N)), dt=g.uniform(-5, 0, size=(T, Dn)),
+                A=-np.exp(g.uniform(0, np.log(16), size=(Dn, N))), D=g.standard_normal(Dn),
+                dt_bias=g.uniform(-2, 1, size=Dn), z=g.standard_normal((T, Dn)))
+
+
+def test_mamba1_with_A_constant_over_n_is_mamba2_with_one_channel_heads():
+    """A Mamba1 layer whose A rows are constant is a Mamba2 layer with D heads of head_dim 1 and
+    one group (scalar A per head): both oracle functions must agree."""
+    pr = _mamba1_problem(60)
+    Dn, N = pr["h"].shape
+    a = -np.exp(_rng(61).uniform(0, 2, size=Dn))
+    A1 = np.repeat(a[:, None], N, axis=1)
+    h1, y1 = oracle.mamba1_update(pr["h"], pr["x"], pr["B"], pr["C"], pr["dt"], A1, D=pr["D"], dt_bias=pr["dt_bias"],
+                                  z=pr["z"])
+    h2, y2 = oracle.ssm_update(pr["h"][:, None, :], pr["x"][:, :, None], pr["B"][:, None, :], pr["C"][:, None, :],
+                               pr["dt"], a, D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"][:, :, None])
+    np.testing.assert_allclose(h1, h2[:, 0, :], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(y1, y2[:, :, 0], rtol=1e-12, atol=1e-14)
+
+
+def test_mamba1_constant_inputs_geometric_series_per_state_channel():
+    """Constant x, B, dt: h_T[d, n] = a^T h_0 + Delta B x (1 - a^T) / (1 - a), a = exp(Delta A[d, n])
+    with a different a for every n."""
+    g = _rng(62)
+    Dn, N, T = 4, 6, 13
+    h0 = g.standard_normal((Dn, N))
+    x1, B1, dt1 = g.standard_normal(Dn), g.standard_normal(N), g.uniform(-3, 0, size=Dn)
+    A = -np.exp(g.uniform(-1, 2, size=(Dn, N)))
+    x, B, C, dt = np.tile(x1, (T, 1)), np.tile(B1, (T, 1)), g.standard_normal((T, N)), np.tile(dt1, (T, 1))
+    hT, y = oracle.mamba1_update(h0, x, B, C, dt, A)
+    delta = np.log1p(np.exp(dt1))
+    a = np.exp(delta[:, None] * A)
+    expect = a ** T * h0 + (delta[:, None] * B1[None, :] * x1[:, None]) * (1 - a ** T) / (1 - a)
+    np.testing.assert_allclose(hT, expect, rtol=1e-12)
+    # the last output reads the last state through C
+    np.testing.assert_allclose(y[-1], hT @ C[-1], rtol=1e-12)
+
+
+def test_mamba1_gate_and_skip():
+    pr = _mamba1_problem(63, T=1)
+    _, y0 = oracle.mamba1_update(pr["h"], pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"])
+    _, yD = oracle.mamba1_update(pr["h"], pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"], D=pr["D"])
+    _, yz = oracle.mamba1_update(pr["h"], pr["x"], pr["B"], pr["C"], pr["dt"], pr["A"], z=pr["z"])
+    np.testing.assert_allclose(yD - y0, pr["D"][None, :] * pr["x"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(yz, y0 * pr["z"] * expit(pr["z"]), rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------------------
 # int8 checkpoint store
 # ----------------------------------------------------------------------------------------
 
