@@ -307,6 +307,34 @@ def _time(torch, fn, steps, warmup, dist=None):
     return e0.elapsed_time(e1) / steps  # ms per step
 
 
+def _time_graph(torch, fn, steps, warmup, dist=None, reps=1):
+    """ms per call of `fn` replayed from a CUDA graph: launch-bound sequences of short kernels are
+    timed on the GPU instead of on the host's launch rate.  `fn` runs eagerly `warmup` times
+    (first-call set-up happens outside the capture), then `reps` calls are captured once and the
+    graph is replayed `steps` times between CUDA events."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1) / (steps * reps)
+
+
 def _max_over_ranks(torch, dist, v, device="cuda"):
     """The slowest rank's time: every rank contributes its own, all get the maximum."""
     if dist is None:
@@ -366,13 +394,15 @@ def run_gpu(args):
     bld.build()
     hbm_peak, bf16_peak, bf16_sus, peak_src = _peaks()
 
-    if args.only in ("prefill", "spec", "sweep", "checkpoint"):
+    if args.only in ("prefill", "spec", "sweep", "checkpoint", "mamba1"):
         if args.only == "prefill":
             res = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
         elif args.only == "spec":
             res = run_spec(torch, args, rank, dist, hbm_peak)
         elif args.only == "checkpoint":
             res = run_checkpoint(torch, args, rank, dist, hbm_peak)
+        elif args.only == "mamba1":
+            res = run_mamba1(torch, args, rank, dist, hbm_peak)
         else:
             res = run_sweep(torch, args, rank, dist, hbm_peak)
         if rank == 0:
@@ -406,7 +436,7 @@ def run_gpu(args):
                "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
     del dec
     torch.cuda.empty_cache()
-    prefill = spec = sweep = ckpt = None
+    prefill = spec = sweep = ckpt = m1 = None
     if args.only == "all":
         prefill = run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak)
         torch.cuda.empty_cache()
@@ -416,6 +446,8 @@ def run_gpu(args):
         torch.cuda.empty_cache()
         ckpt = run_checkpoint(torch, args, rank, dist, hbm_peak)
         torch.cuda.empty_cache()
+        m1 = run_mamba1(torch, args, rank, dist, hbm_peak)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and args.only == "all" and not args.no_cpu_baseline:
@@ -423,7 +455,7 @@ def run_gpu(args):
 
     if rank == 0:
         emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck,
-             prefill, cpu, spec, sweep, ckpt)
+             prefill, cpu, spec, sweep, ckpt, m1)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -514,11 +546,76 @@ def run_sweep(torch, args, rank, dist, hbm_peak):
             bd.mamba_state_update(desc, ssm, slot, xbc, dt, prm["A"], y, conv_pool=conv, conv_w=prm["conv_w"],
                                   D=prm["D"], dt_bias=prm["dt_bias"], z=z)
 
-        ms = _max_over_ranks(torch, dist, _time(torch, step, max(args.steps, 20), max(args.warmup, 3), dist))
+        # a graph of 16 launches replayed: small batches are timed on the GPU, not on the host's launch rate
+        ms = _max_over_ranks(torch, dist, _time_graph(torch, step, max(args.steps // 4, 10), max(args.warmup, 3), dist,
+                                                      reps=16))
         gbs = live * DECODE_BYTES_PER_TOKEN_LAYER / (ms * 1e-3) / 1e9
         out.append({"batch": batch, "live_rows": live, "us_per_launch": ms * 1e3, "gbs": gbs,
                     "hbm_frac": gbs / hbm_peak})
-    return {"workload": SWEEP["name"], "points": out}
+    return {"workload": SWEEP["name"], "launch": "CUDA graph replay (16 launches per graph)", "points": out}
+
+
+M1 = wl.MAMBA1_DECODE
+M1D, M1N, M1W = M1["d_inner"], M1["d_state"], M1["conv_kernel"]
+# Mamba1 decode, per token-layer (bf16): state read + write, conv state read + write, x into the
+# conv, its output written and read by the update, z in, y out, dt (fp32), B and C
+M1_BYTES_PER_TOKEN_LAYER = 2 * M1D * M1N * 2 + 2 * M1D * (M1W - 1) * 2 + 5 * M1D * 2 + M1D * 4 + 2 * M1N * 2
+# the state-update kernel alone: state read + write, x, z, y, dt, B, C
+M1_UPDATE_BYTES = 2 * M1D * M1N * 2 + 3 * M1D * 2 + M1D * 4 + 2 * M1N * 2
+
+
+def run_mamba1(torch, args, rank, dist, hbm_peak):
+    """Mamba1 decode: every layer runs the conv update then the state update for batch 256 of a
+    512-slot pool (bf16), 64 layers per step; the state-update kernel is also timed alone."""
+    from recurrent_state_update_gb300 import binding as bd
+    dev = torch.device("cuda")
+    bf = torch.bfloat16
+    L, batch, S = args.layers or M1["layers"], M1["batch"], M1["pool"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(M1["seed"] * 1000 + rank)
+    ssm = [torch.randn(S, M1D, M1N, generator=gen, device=dev).mul_(0.1).to(bf) for _ in range(L)]
+    conv = [torch.randn(S, M1D, M1W - 1, generator=gen, device=dev).mul_(0.1).to(bf) for _ in range(L)]
+    g = wl.rng(M1["seed"] * 1000 + rank, 0)
+    prm_np = wl.mamba1_params(g, M1D, M1N, M1W)
+    prm = {k: torch.from_numpy(v).to(dev) for k, v in prm_np.items()}
+    inp = wl.mamba1_inputs(g, prm_np, batch, M1N, wl.BF16)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(bf)
+    x_in = to(inp["x"]).view(batch, 1, M1D)
+    x_c = torch.empty(batch, 1, M1D, dtype=bf, device=dev)
+    B, C, z = to(inp["B"]), to(inp["C"]), to(inp["z"])
+    dt = torch.from_numpy(inp["dt"]).to(dev)
+    y = torch.empty(batch, M1D, dtype=bf, device=dev)
+    slot = torch.from_numpy(wl.slot_ids(g, S, batch)).to(dev)
+    desc = bd.mamba1_desc(M1D, M1N, M1W)
+
+    def update(l):
+        bd.mamba1_state_update(desc, ssm[l], slot, x_c.view(batch, M1D), dt, prm["A"], B, C, y, D=prm["D"],
+                               dt_bias=prm["dt_bias"], z=z)
+
+    def step():
+        for l in range(L):
+            bd.mamba1_conv_update(desc, conv[l], slot, x_in, prm["conv_w"], x_c)
+            update(l)
+
+    def updates():
+        for l in range(L):
+            update(l)
+
+    # 128 short launches per step: timed from a CUDA graph (the host's launch rate would dominate)
+    ms = _max_over_ranks(torch, dist, _time_graph(torch, step, max(args.steps // 4, 10), max(args.warmup, 3), dist))
+    ms_u = _max_over_ranks(torch, dist, _time_graph(torch, updates, max(args.steps // 4, 10), max(args.warmup, 3),
+                                                    dist))
+    by = L * batch * M1_BYTES_PER_TOKEN_LAYER
+    by_u = L * batch * M1_UPDATE_BYTES
+    out = {"workload": M1["name"], "ms_per_step": ms, "gbs": by / (ms * 1e-3) / 1e9,
+           "hbm_frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "token_layers_per_s": L * batch / (ms * 1e-3),
+           "algorithmic_bytes_per_token_layer": M1_BYTES_PER_TOKEN_LAYER, "launches_per_step": 2 * L,
+           "launch": "CUDA graph replay (one graph per step)",
+           "state_update": {"kernel": "k_mamba1_update", "us_per_launch": ms_u * 1e3 / L,
+                            "gbs": by_u / (ms_u * 1e-3) / 1e9, "hbm_frac": by_u / (ms_u * 1e-3) / 1e9 / hbm_peak,
+                            "algorithmic_bytes_per_launch": batch * M1_UPDATE_BYTES}}
+    del ssm, conv
+    return out
 
 
 CKPT_ROWS = 256  # slots restored, stored or loaded per call
@@ -590,7 +687,7 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
 
 
 def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
-         cpu, spec=None, sweep=None, ckpt=None):
+         cpu, spec=None, sweep=None, ckpt=None, m1=None):
     line = {
         "metric": "decode state-update GB/s (and token-layers/s) vs HBM peak; prefill tokens/s",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -613,6 +710,7 @@ def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_
         "spec_decode": spec,
         "padding_sweep": sweep,
         "checkpoint": ckpt,
+        "mamba1_decode": m1,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -677,7 +775,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--layers", type=int, default=0, help="decode layers per step (default: the workload's 48)")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "spec", "sweep", "checkpoint"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "spec", "sweep", "checkpoint", "mamba1"],
+                    default="all",
                     help="time one form alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps

@@ -371,6 +371,58 @@ int mamba_chunk_scan_noalloc(const mamba_layer_desc *desc, void *ssm_pool, int64
 /* Size in bytes of the fixed scratch mamba_chunk_scan_noalloc uses (no counterpart on the pages). */
 size_t mamba_chunk_scan_static_scratch_bytes(void);
 
+/* ---------------------------------------------------------------------------------------- */
+/* Mamba1 (S6) layers                                                                        */
+/* ---------------------------------------------------------------------------------------- */
+
+/* One Mamba1 layer [P1: the Mamba1 conv state (D, W-1) and recurrent state (D, N); P4 the Mamba
+ * block equations, with a step and a row of A per channel]. */
+typedef struct mamba1_layer_desc {
+    int32_t d_inner;     /* D, the channels; a multiple of 8 */
+    int32_t d_state;     /* N: 8, 16, 32 or 64 */
+    int32_t conv_kernel; /* W, 2..8 */
+    int32_t num_spec;    /* extra conv-state columns, >= 0 */
+    int32_t state_dtype; /* mamba_dtype of the (D, N) state pool */
+    int32_t conv_dtype;  /* mamba_dtype of the conv state pool; must equal act_dtype */
+    int32_t act_dtype;   /* mamba_dtype of x, B, C, z and y */
+    int32_t dt_dtype;    /* mamba_dtype of dt */
+} mamba1_layer_desc;
+
+/*
+ * mamba1_conv_update -- the causal depthwise conv1d + SiLU of a Mamba1 layer over ntok new tokens
+ * per request (the D channels of x; B, C and the step are projected from its output outside this
+ * library), with the conv state updated in place.  Same semantics, layouts and limits as
+ * mamba_conv_update with conv_dim = d_inner.
+ */
+int mamba1_conv_update(const mamba1_layer_desc *desc, void *conv_pool, int64_t conv_slot_stride,
+                       int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
+                       const void *x_in, const float *conv_w, const float *conv_b, void *x_out,
+                       int32_t *err_word, void *stream);
+
+/*
+ * mamba1_state_update -- the batched single-token decode step of a Mamba1 layer [P4: h_t =
+ * exp(Delta_t A) h_{t-1} + Delta_t B_t x_t, y_t = C_t h_t (+ D x_t), y_hat = y (.) SiLU(z); P1 the
+ * (D, N) state in a slot pool].  For each row i with s = slot_ids[i] != -1 and each channel d:
+ *     Delta = softplus(dt[i, d] + dt_bias[d])   (dt + dt_bias when dt_softplus == 0)
+ *     h[d, n] <- exp(Delta * A[d, n]) * h[d, n] + Delta * B[i, n] * x[i, d]
+ *     y[i, d] = sum_n C[i, n] * h[d, n] + D[d] * x[i, d];   y *= SiLU(z[i, d]) if z
+ *   ssm_pool    slot s at ssm_pool + s*ssm_slot_stride elements: (d_inner, d_state) state_dtype,
+ *               d_state contiguous; read, updated in fp32 and written back (bf16: RNE).
+ *   slot_ids    (batch) int32, -1 = padding (row skipped, y row not written).
+ *   x           (batch, d_inner) act_dtype, the conv output.
+ *   dt          (batch, d_inner) dt_dtype.
+ *   A           (d_inner, d_state) fp32, required.   D, dt_bias: (d_inner) fp32 or NULL.
+ *   B, C        (batch, d_state) act_dtype.
+ *   z, y        (batch, d_inner) act_dtype (z may be NULL).
+ * Alignment: ssm_pool and the slot stride in bytes multiples of 16, the other tensors aligned to
+ * their element size.  Limits: batch <= 65535.
+ */
+int mamba1_state_update(const mamba1_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
+                        int64_t num_slots, const int32_t *slot_ids, int32_t batch, const void *x,
+                        const void *dt, const float *A, const void *B, const void *C, const float *D,
+                        const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
+                        int32_t *err_word, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

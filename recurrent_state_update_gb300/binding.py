@@ -38,6 +38,19 @@ class LayerDesc(ctypes.Structure):
                                               "dt_dtype")]
 
 
+class Mamba1Desc(ctypes.Structure):
+    """Mirror of ``mamba1_layer_desc``."""
+
+    _fields_ = [(n, ctypes.c_int32) for n in ("d_inner", "d_state", "conv_kernel", "num_spec", "state_dtype",
+                                              "conv_dtype", "act_dtype", "dt_dtype")]
+
+
+def mamba1_desc(d_inner: int, d_state: int, conv_kernel: int = 4, num_spec: int = 0, state: str = wl.BF16,
+                act: str = wl.BF16, dt: str = wl.F32) -> Mamba1Desc:
+    code = wl.DTYPE_CODE
+    return Mamba1Desc(d_inner, d_state, conv_kernel, num_spec, code[state], code[act], code[act], code[dt])
+
+
 def layer_desc(shape: "wl.LayerShape", state: str = wl.BF16, act: str = wl.BF16, dt: str = wl.F32,
                conv: str | None = None) -> LayerDesc:
     code = wl.DTYPE_CODE
@@ -49,6 +62,7 @@ _lock = threading.Lock()
 _lib = None
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 _dp = ctypes.POINTER(LayerDesc)
+_d1 = ctypes.POINTER(Mamba1Desc)
 
 # (name, restype, argtypes) of every exported entry point
 SIGNATURES = {
@@ -63,6 +77,9 @@ SIGNATURES = {
     "mamba_spec_commit": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
     "mamba_conv_varlen": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
+    "mamba1_conv_update": (ctypes.c_int, [_d1, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mamba1_state_update": (ctypes.c_int, [_d1, _vp, _i64, _i64, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                           _vp, _vp, _vp, _vp]),
     "mamba_slot_copy": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _i32, _vp, _vp]),
     "mamba_int8_entry_bytes": (_sz, [_dp]),
     "mamba_ckpt_store_int8": (ctypes.c_int, [_dp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i64, _vp, _vp]),
@@ -183,6 +200,31 @@ def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept
                                  _ptr(conv_pool), conv_stride, _cptr(slot_ids), _cptr(scratch_slots),
                                  _cptr(accept_len), batch, ntok, _ptr(err_word), _stream(stream))
     _check(rc, "mamba_spec_commit")
+
+
+# ------------------------------------------------------------------------------------------
+# Mamba1 (S6) layers
+# ------------------------------------------------------------------------------------------
+
+def mamba1_conv_update(desc: Mamba1Desc, conv_pool, slot_ids, x_in, conv_w, x_out, *, conv_b=None, err_word=None,
+                       stream=None):
+    """Causal conv1d + SiLU of a Mamba1 layer over (batch, ntok, d_inner) inputs, conv state in place."""
+    batch, ntok = int(slot_ids.shape[0]), int(x_in.shape[1])
+    rc = lib().mamba1_conv_update(ctypes.byref(desc), _ptr(conv_pool), conv_pool.stride(0), conv_pool.shape[0],
+                                  _cptr(slot_ids), batch, ntok, _cptr(x_in), _cptr(conv_w), _cptr(conv_b),
+                                  _cptr(x_out), _ptr(err_word), _stream(stream))
+    _check(rc, "mamba1_conv_update")
+
+
+def mamba1_state_update(desc: Mamba1Desc, ssm_pool, slot_ids, x, dt, A, B, C, y, *, D=None, dt_bias=None,
+                        dt_softplus=True, z=None, err_word=None, stream=None):
+    """The batched single-token Mamba1 decode step, in place on the (slots, d_inner, d_state) pool."""
+    batch = int(slot_ids.shape[0])
+    rc = lib().mamba1_state_update(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
+                                   _cptr(slot_ids), batch, _cptr(x), _cptr(dt), _cptr(A), _cptr(B), _cptr(C), _cptr(D),
+                                   _cptr(dt_bias), int(bool(dt_softplus)), _cptr(z), _cptr(y), _ptr(err_word),
+                                   _stream(stream))
+    _check(rc, "mamba1_state_update")
 
 
 # ------------------------------------------------------------------------------------------

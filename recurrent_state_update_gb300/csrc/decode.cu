@@ -791,6 +791,110 @@ struct ConvArgs {
     int W, Wc, Cd;
 };
 
+// Single-token conv step for a window of exactly W-1 columns: one thread per 16-byte vector of
+// channels (V = 8 bf16 or 4 fp32) and kConvRows batch rows.  The vector's taps (V x W fp32,
+// contiguous) are loaded once as 16-byte vectors and reused for the rows; a slot keeps each
+// channel's W-1 columns contiguous, so the vector's window is W-1 contiguous 16-byte loads.  All
+// rows' loads are issued before any arithmetic; the new windows (shifted by one, the token
+// appended) and the outputs are written back as 16-byte stores.
+constexpr int kConvRows = 4;
+
+template <typename ActT, int W>
+__global__ void __launch_bounds__(256) k_conv_step(const ConvArgs a, int batch) {
+    constexpr int V = Vec16<ActT>::n;
+    const int c0 = (blockIdx.x * 256 + threadIdx.x) * V;
+    if (c0 >= a.Cd) return;
+    float wv[V * W];  // wv[v * W + k]: tap k of channel c0 + v
+#pragma unroll
+    for (int q = 0; q < V * W / 4; ++q) {
+        const float4 t = reinterpret_cast<const float4 *>(a.w + (int64_t)c0 * W)[q];
+        wv[4 * q] = t.x;
+        wv[4 * q + 1] = t.y;
+        wv[4 * q + 2] = t.z;
+        wv[4 * q + 3] = t.w;
+    }
+    float bv[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) bv[v] = a.b ? a.b[c0 + v] : 0.0f;
+    const int i0 = blockIdx.y * kConvRows;
+    uint4 raw[kConvRows][W];  // [r][k < W-1]: the slot's window vectors, [r][W-1]: the token
+    ActT *st[kConvRows];
+#pragma unroll
+    for (int r = 0; r < kConvRows; ++r) {
+        st[r] = nullptr;
+        const int i = i0 + r;
+        if (i >= batch) continue;
+        const int32_t s = a.slot[i];
+        if (s < 0) continue;
+        if (s >= a.num_slots) {
+            if (c0 == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+            continue;
+        }
+        st[r] = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride + (int64_t)c0 * (W - 1);
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) raw[r][k] = reinterpret_cast<const uint4 *>(st[r])[k];
+        raw[r][W - 1] = *reinterpret_cast<const uint4 *>(static_cast<const ActT *>(a.xbc_in) + (int64_t)i * a.Cd + c0);
+    }
+#pragma unroll
+    for (int r = 0; r < kConvRows; ++r) {
+        if (!st[r]) continue;
+        // cur[v * (W-1) + c]: column c (oldest first) of channel c0 + v (the slot's channel-major
+        // order); x[v]: the token
+        float cur[V * (W - 1)], x[V];
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) {
+            float f[V];
+            unpack16(raw[r][k], f);
+#pragma unroll
+            for (int e = 0; e < V; ++e) cur[k * V + e] = f[e];
+        }
+        unpack16(raw[r][W - 1], x);
+        float o[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float acc = fmaf(wv[v * W + W - 1], x[v], bv[v]);
+#pragma unroll
+            for (int c = 0; c < W - 1; ++c) acc = fmaf(wv[v * W + c], cur[v * (W - 1) + c], acc);
+            o[v] = silu_f(acc);
+        }
+        *reinterpret_cast<uint4 *>(static_cast<ActT *>(a.xbc_out) + (int64_t)(i0 + r) * a.Cd + c0) = pack16(o);
+        // new window: every channel's columns shifted left by one, the token appended
+        float nw[V * (W - 1)];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+#pragma unroll
+            for (int c = 0; c + 1 < W - 1; ++c) nw[v * (W - 1) + c] = cur[v * (W - 1) + c + 1];
+            nw[v * (W - 1) + W - 2] = x[v];
+        }
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) {
+            float f[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) f[e] = nw[k * V + e];
+            reinterpret_cast<uint4 *>(st[r])[k] = pack16(f);
+        }
+    }
+}
+
+// Launches the single-token conv step when it applies (ntok 1, a window of W-1 columns, 16-byte
+// aligned vectors); false when the general kernel must run instead.
+template <typename ActT>
+bool launch_conv_step(const ConvArgs &a, int batch, size_t ab, cudaStream_t st) {
+    constexpr int V = Vec16<ActT>::n;
+    if (a.ntok != 1 || a.Wc != a.W - 1 || a.Cd % V || !aligned16(a.conv_pool) || !aligned16(a.xbc_in) ||
+        !aligned16(a.xbc_out) || !aligned16(a.w) || ((size_t)a.conv_stride * ab) % 16)
+        return false;
+    const dim3 grid((a.Cd / V + 255) / 256, (batch + kConvRows - 1) / kConvRows);
+    switch (a.W) {
+        case 2: k_conv_step<ActT, 2><<<grid, 256, 0, st>>>(a, batch); break;
+        case 3: k_conv_step<ActT, 3><<<grid, 256, 0, st>>>(a, batch); break;
+        case 4: k_conv_step<ActT, 4><<<grid, 256, 0, st>>>(a, batch); break;
+        case 5: k_conv_step<ActT, 5><<<grid, 256, 0, st>>>(a, batch); break;
+        default: return false;
+    }
+    return true;
+}
+
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_conv_update(const ConvArgs a) {
     const int cb = blockIdx.x, i = blockIdx.y, ntok = a.ntok;
@@ -1057,10 +1161,45 @@ extern "C" int mamba_conv_update(const mamba_layer_desc *d, void *conv_pool, int
     a.conv_pool = conv_pool; a.conv_stride = conv_slot_stride; a.num_slots = num_slots;
     a.slot = slot_ids; a.ntok = ntok; a.xbc_in = xbc_in; a.w = conv_w; a.b = conv_b;
     a.xbc_out = xbc_out; a.err = err_word; a.W = d->conv_kernel; a.Wc = Wc; a.Cd = Cd;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d->act_dtype == MAMBA_BF16 ? launch_conv_step<bf16>(a, batch, ab, st) : launch_conv_step<float>(a, batch, ab, st))
+        return launch_status();
     const size_t smem = sizeof(float) * 2 * (size_t)ntok * CONV_CHANNELS + ab * (size_t)CONV_CHANNELS * Wc;
     if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
     const dim3 grid((Cd + CONV_CHANNELS - 1) / CONV_CHANNELS, batch), block(256);
+    auto kern = d->act_dtype == MAMBA_BF16 ? k_conv_update<bf16> : k_conv_update<float>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MAMBA_ECUDA;
+    kern<<<grid, block, smem, st>>>(a);
+    return launch_status();
+}
+
+extern "C" int mamba1_conv_update(const mamba1_layer_desc *d, void *conv_pool, int64_t conv_slot_stride,
+                                  int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
+                                  const void *x_in, const float *conv_w, const float *conv_b, void *x_out,
+                                  int32_t *err_word, void *stream) {
+    if (!d || d->d_inner <= 0 || d->conv_kernel < 2 || d->conv_kernel > 8 || d->num_spec < 0 || d->num_spec > 32 ||
+        !dtype_ok(d->act_dtype) || !dtype_ok(d->conv_dtype))
+        return MAMBA_EINVAL;
+    if (batch < 0 || batch > 65535 || ntok < 1 || ntok > 64) return MAMBA_EINVAL;
+    if (batch == 0) return MAMBA_OK;
+    if (!conv_pool || !slot_ids || !x_in || !conv_w || !x_out) return MAMBA_EINVAL;
+    if (d->conv_dtype != d->act_dtype) return MAMBA_EUNSUPPORTED;
+    const int Cd = d->d_inner, Wc = d->conv_kernel - 1 + d->num_spec;
+    if (num_slots <= 0 || conv_slot_stride < (int64_t)Cd * Wc) return MAMBA_EINVAL;
+    const size_t ab = dtype_bytes(d->act_dtype);
+    if (((uintptr_t)conv_pool | (uintptr_t)x_in | (uintptr_t)x_out) % ab != 0) return MAMBA_EALIGN;
+    ConvArgs a;
+    a.conv_pool = conv_pool; a.conv_stride = conv_slot_stride; a.num_slots = num_slots;
+    a.slot = slot_ids; a.ntok = ntok; a.xbc_in = x_in; a.w = conv_w; a.b = conv_b;
+    a.xbc_out = x_out; a.err = err_word; a.W = d->conv_kernel; a.Wc = Wc; a.Cd = Cd;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d->act_dtype == MAMBA_BF16 ? launch_conv_step<bf16>(a, batch, ab, st) : launch_conv_step<float>(a, batch, ab, st))
+        return launch_status();
+    const size_t smem = sizeof(float) * 2 * (size_t)ntok * CONV_CHANNELS + ab * (size_t)CONV_CHANNELS * Wc;
+    if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
+    const dim3 grid((Cd + CONV_CHANNELS - 1) / CONV_CHANNELS, batch), block(256);
     auto kern = d->act_dtype == MAMBA_BF16 ? k_conv_update<bf16> : k_conv_update<float>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

@@ -74,6 +74,11 @@ SPEC_DECODE = dict(name="speculative decode, batch 128, 4 draft tokens, 4 scratc
                    shape=NEMOTRON_H_8B.with_spec(4), batch=128, ntok=4, state=BF16, act=BF16, seed=4)
 
 
+MAMBA1_DECODE = dict(name="Mamba1 (S6) decode, Mamba-2.8B-like layers (d_inner 5120, d_state 16, W 4), 64 layers, "
+                          "batch 256 of 512 slots, bf16 state",
+                     d_inner=5120, d_state=16, conv_kernel=4, layers=64, batch=256, pool=512, seed=6)
+
+
 def rng(*key: int) -> np.random.Generator:
     """PCG64 stream for a (config seed, layer, step, ...) key."""
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(k) for k in key])))
@@ -217,6 +222,26 @@ def prefill_inputs(g: np.random.Generator, shape: LayerShape, params: dict, T: i
 def prefill_xbc(g: np.random.Generator, shape: LayerShape, T: int, act: str) -> np.ndarray:
     """Raw (pre-conv) prefill rows xBC (T, conv_dim), distributed like the decode inputs."""
     return store(xbc_values(g, shape, (T,)), act)
+
+
+def mamba1_params(g: np.random.Generator, d_inner: int, d_state: int, conv_kernel: int) -> dict:
+    """Mamba1 layer parameters: A (D, N) = -exp(U(ln 1, ln 16)), D, dt_bias (per channel), conv taps."""
+    A = -np.exp(g.uniform(math.log(1.0), math.log(16.0), size=(d_inner, d_state)))
+    D = g.standard_normal(d_inner)
+    u = np.exp(g.uniform(math.log(0.005), math.log(0.02), size=d_inner))
+    conv_w = g.standard_normal((d_inner, conv_kernel)) / 2.0
+    return dict(A=store(A, F32), D=store(D, F32), dt_bias=store(_inv_softplus(u), F32), conv_w=store(conv_w, F32))
+
+
+def mamba1_inputs(g: np.random.Generator, params: dict, batch: int, d_state: int, act: str) -> dict:
+    """One Mamba1 decode step: x (conv output) and z N(0,1), B, C N(0,1)/sqrt(N), raw dt fp32."""
+    Dn = params["D"].shape[0]
+    x = store(g.standard_normal((batch, Dn)), act)
+    B = store(g.standard_normal((batch, d_state)) / math.sqrt(d_state), act)
+    C = store(g.standard_normal((batch, d_state)) / math.sqrt(d_state), act)
+    dt = store(raw_dt(g, params["dt_bias"], (batch,)), F32)
+    z = store(g.standard_normal((batch, Dn)), act)
+    return dict(x=x, B=B, C=C, dt=dt, z=z)
 
 
 def accept_lengths(g: np.random.Generator, batch: int, ntok: int) -> np.ndarray:

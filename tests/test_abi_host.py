@@ -231,3 +231,22 @@ def test_checkpoint_ops_host_errors(lib):
     odd = bd.layer_desc(wl.LayerShape(nheads=2, head_dim=4, d_state=12, n_groups=1, conv_kernel=4))
     assert lib.mamba_ckpt_store_int8(ctypes.byref(odd), FAKE, 96, None, 0, 8, FAKE, FAKE, 4, FAKE, 4, None,
                                      None) == bd.MAMBA_EUNSUPPORTED
+
+
+def test_mamba1_host_errors(lib):
+    d = bd.mamba1_desc(5120, 16)
+    st = 5120 * 16
+
+    def call(dd=d, pool=FAKE, stride=st, A=FAKE, x=FAKE):
+        return lib.mamba1_state_update(ctypes.byref(dd), pool, stride, 8, FAKE, 4, x, FAKE, A, FAKE, FAKE, None,
+                                       None, 1, None, FAKE, None, None)
+
+    assert call(pool=None) == bd.MAMBA_EINVAL
+    assert call(A=None) == bd.MAMBA_EINVAL
+    assert call(stride=st - 1) == bd.MAMBA_EINVAL
+    assert call(pool=FAKE + 2) == bd.MAMBA_EALIGN
+    assert call(x=FAKE + 1) == bd.MAMBA_EALIGN
+    assert call(dd=bd.mamba1_desc(5120, 12)) == bd.MAMBA_EUNSUPPORTED
+    assert call(dd=bd.mamba1_desc(5121, 16)) == bd.MAMBA_EINVAL
+    r = lib.mamba1_conv_update(ctypes.byref(d), None, 5120 * 3, 8, FAKE, 4, 1, FAKE, FAKE, None, FAKE, None, None)
+    assert r == bd.MAMBA_EINVAL
