@@ -792,17 +792,19 @@ struct ConvArgs {
 };
 
 // Single-token conv step for a window of exactly W-1 columns: one thread per 16-byte vector of
-// channels (V = 8 bf16 or 4 fp32) and kConvRows batch rows.  The vector's taps (V x W fp32,
+// channels (V = 8 bf16 or 4 fp32) and kConvRows batch rows, in small blocks so that a batch
+// launches many of them.  The vector's taps (V x W fp32,
 // contiguous) are loaded once as 16-byte vectors and reused for the rows; a slot keeps each
 // channel's W-1 columns contiguous, so the vector's window is W-1 contiguous 16-byte loads.  All
 // rows' loads are issued before any arithmetic; the new windows (shifted by one, the token
 // appended) and the outputs are written back as 16-byte stores.
-constexpr int kConvRows = 4;
+constexpr int kConvRows = 2;
+constexpr int kConvThreads = 128;
 
 template <typename ActT, int W>
-__global__ void __launch_bounds__(256) k_conv_step(const ConvArgs a, int batch) {
+__global__ void __launch_bounds__(kConvThreads) k_conv_step(const ConvArgs a, int batch) {
     constexpr int V = Vec16<ActT>::n;
-    const int c0 = (blockIdx.x * 256 + threadIdx.x) * V;
+    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
     if (c0 >= a.Cd) return;
     float wv[V * W];  // wv[v * W + k]: tap k of channel c0 + v
 #pragma unroll
@@ -884,12 +886,12 @@ bool launch_conv_step(const ConvArgs &a, int batch, size_t ab, cudaStream_t st) 
     if (a.ntok != 1 || a.Wc != a.W - 1 || a.Cd % V || !aligned16(a.conv_pool) || !aligned16(a.xbc_in) ||
         !aligned16(a.xbc_out) || !aligned16(a.w) || ((size_t)a.conv_stride * ab) % 16)
         return false;
-    const dim3 grid((a.Cd / V + 255) / 256, (batch + kConvRows - 1) / kConvRows);
+    const dim3 grid((a.Cd / V + kConvThreads - 1) / kConvThreads, (batch + kConvRows - 1) / kConvRows);
     switch (a.W) {
-        case 2: k_conv_step<ActT, 2><<<grid, 256, 0, st>>>(a, batch); break;
-        case 3: k_conv_step<ActT, 3><<<grid, 256, 0, st>>>(a, batch); break;
-        case 4: k_conv_step<ActT, 4><<<grid, 256, 0, st>>>(a, batch); break;
-        case 5: k_conv_step<ActT, 5><<<grid, 256, 0, st>>>(a, batch); break;
+        case 2: k_conv_step<ActT, 2><<<grid, kConvThreads, 0, st>>>(a, batch); break;
+        case 3: k_conv_step<ActT, 3><<<grid, kConvThreads, 0, st>>>(a, batch); break;
+        case 4: k_conv_step<ActT, 4><<<grid, kConvThreads, 0, st>>>(a, batch); break;
+        case 5: k_conv_step<ActT, 5><<<grid, kConvThreads, 0, st>>>(a, batch); break;
         default: return false;
     }
     return true;
