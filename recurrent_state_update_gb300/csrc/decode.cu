@@ -136,6 +136,96 @@ __device__ __forceinline__ void conv_phase(const ChanRanges &cr, ActT *cstate, i
     }
 }
 
+// Element e of a register array of 16-byte vectors holding raw 16-bit (PW = 2) or 32-bit (PW = 1)
+// values; e is a compile-time constant once the callers' loops are unrolled.
+template <int PW, int K>
+__device__ __forceinline__ uint32_t raw_at(const uint4 (&a)[K], int e) {
+    const int wi = e / PW;
+    const uint4 &q = a[wi / 4];
+    const int c = wi % 4;
+    const uint32_t w = c == 0 ? q.x : (c == 1 ? q.y : (c == 2 ? q.z : q.w));
+    if (PW == 1) return w;
+    return (e & 1) ? (w >> 16) : (w & 0xffffu);
+}
+
+template <int PW>
+__device__ __forceinline__ float raw_f32(uint32_t r) {
+    return PW == 1 ? __uint_as_float(r) : __uint_as_float(r << 16);
+}
+
+__device__ __forceinline__ void set_word(uint4 &q, int c, uint32_t w) {
+    if (c == 0) q.x = w;
+    else if (c == 1) q.y = w;
+    else if (c == 2) q.z = w;
+    else q.w = w;
+}
+
+// Conv phase of one 16-byte vector of channels (V channels, local channels lc0 .. lc0 + V - 1) for
+// NTK tokens with a W-tap kernel and a window of exactly W-1+NTK columns: the vector's window is
+// W-1+NTK contiguous 16-byte loads (a slot keeps each channel's columns together), every load is
+// issued before any arithmetic, and the new window (the last W-1+NTK entries of [old window |
+// tokens]) is assembled from the raw values, so the conv state stays bit-exact.
+template <typename ActT, int W, int NTK>
+__device__ __forceinline__ void conv_phase_vec(const ChanRanges &cr, ActT *cstate, const ActT *u_row, int Cd,
+                                               const float *__restrict__ w, const float *__restrict__ b,
+                                               float *xs, int lc0) {
+    constexpr int V = Vec16<ActT>::n, PW = (int)(4 / sizeof(ActT)), WC = W - 1 + NTK;
+    const int LC = cr.total;
+    const int c0 = local_to_global(cr, lc0);
+    uint4 *sp = reinterpret_cast<uint4 *>(cstate + (int64_t)c0 * WC);
+    uint4 win[WC], tok[NTK];
+#pragma unroll
+    for (int k = 0; k < WC; ++k) win[k] = sp[k];
+#pragma unroll
+    for (int j = 0; j < NTK; ++j) tok[j] = *reinterpret_cast<const uint4 *>(u_row + (int64_t)j * Cd + c0);
+    float wv[V * W];  // wv[v * W + k]: tap k of channel c0 + v
+#pragma unroll
+    for (int q = 0; q < V * W / 4; ++q) {
+        const float4 t = reinterpret_cast<const float4 *>(w + (int64_t)c0 * W)[q];
+        wv[4 * q] = t.x;
+        wv[4 * q + 1] = t.y;
+        wv[4 * q + 2] = t.z;
+        wv[4 * q + 3] = t.w;
+    }
+    float bv[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) bv[v] = b ? b[c0 + v] : 0.0f;
+    // input m of [old window (WC) | tokens (NTK)] for channel v
+    auto input = [&](int v, int m) -> uint32_t {
+        return m < WC ? raw_at<PW>(win, v * WC + m) : raw_at<PW>(tok, (m - WC) * V + v);
+    };
+#pragma unroll
+    for (int j = 0; j < NTK; ++j) {
+        float o[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float acc = bv[v];
+#pragma unroll
+            for (int k = 0; k < W; ++k) acc = fmaf(wv[v * W + k], raw_f32<PW>(input(v, WC + j - (W - 1) + k)), acc);
+            o[v] = silu_f(acc);
+        }
+        float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)j * LC + lc0);
+#pragma unroll
+        for (int q = 0; q < V / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+    uint4 nw[WC];
+#pragma unroll
+    for (int wi = 0; wi < WC * 4; ++wi) {  // 32-bit words of the new window
+        uint32_t word;
+        if (PW == 1) {
+            const int e = wi, v = e / WC, k = e - v * WC;
+            word = input(v, NTK + k);
+        } else {
+            const int e0 = 2 * wi, e1 = e0 + 1;
+            const int v0 = e0 / WC, k0 = e0 - v0 * WC, v1 = e1 / WC, k1 = e1 - v1 * WC;
+            word = input(v0, NTK + k0) | (input(v1, NTK + k1) << 16);
+        }
+        set_word(nw[wi / 4], wi % 4, word);
+    }
+#pragma unroll
+    for (int k = 0; k < WC; ++k) sp[k] = nw[k];
+}
+
 // ---------------------------------------------------------------------------------------
 // fused decode kernel
 // ---------------------------------------------------------------------------------------
@@ -158,24 +248,49 @@ struct DecodeArgs {
     int32_t *err;
     int H, G, HG, W, Wc, Cd;
     int sps;  // state-tile stages per head slot
+    int vec;  // 16-byte vectorised conv / output phases (see DecodeSmem)
 };
 
 // Bound on the polls of one mbarrier wait (a copy that never lands is reported, not waited on forever).
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr int kFlagWords = 16;
 
-// Shared-memory floats after the tile stages, barriers and flags (the conv staging area follows, in ActT).
-__host__ __device__ inline int decode_smem_floats(int ntok, int LC, int HG, int P, bool conv) {
-    return ntok * LC + (conv ? ntok * LC : 0) + 2 * ntok * HG + ntok * HG * P;
-}
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
-// Byte offset of the float area: after S tile stages and S mbarriers (padded to 16 bytes) and the flags.
-__host__ __device__ inline size_t decode_float_offset(int S, size_t tile_bytes) {
-    return (size_t)S * tile_bytes + (((size_t)S * 8 + 15) & ~(size_t)15) + sizeof(int) * kFlagWords;
-}
+// Shared-memory map of k_decode (byte offsets): S tile stages, S + 1 mbarriers (the last one for
+// the z rows), the flags, then the per-row areas.  The vectorised form (vec) keeps the conv window
+// in registers and stages the row's z values; the general form stages the old conv state and the
+// raw inputs instead.
+struct DecodeSmem {
+    size_t bars, flags, xs, uraw, dl, da, ys, dh, scr, cs, zs, total;
+    __host__ __device__ DecodeSmem(int S, size_t tile, int ntok, int LC, int HG, int P, int Wc, size_t es, bool conv,
+                                   bool vec) {
+        bars = (size_t)S * tile;
+        flags = align16(bars + 8 * (size_t)(S + 1));
+        size_t o = flags + sizeof(int) * kFlagWords;
+        xs = o;    o = align16(o + sizeof(float) * (size_t)ntok * LC);     // [ntok][LC] x | B | C after the conv
+        uraw = o;  if (conv && !vec) o = align16(o + sizeof(float) * (size_t)ntok * LC);  // raw inputs
+        dl = o;    o = align16(o + sizeof(float) * (size_t)ntok * HG);     // [ntok][HG] Delta
+        da = o;    o = align16(o + sizeof(float) * (size_t)ntok * HG);     // [ntok][HG] exp(Delta*A)
+        ys = o;    o = align16(o + sizeof(float) * (size_t)ntok * HG * P); // [ntok][HG*P] C.h
+        dh = o;    o = align16(o + sizeof(float) * (size_t)HG);            // D of the group's heads
+        scr = o;   o = align16(o + sizeof(int) * (size_t)ntok);            // the row's scratch slots
+        cs = o;    if (conv && !vec) o = align16(o + es * (size_t)LC * Wc);  // old conv state
+        zs = o;    if (vec) o = align16(o + es * (size_t)ntok * HG * P);   // [ntok][HG*P] z
+        total = o;
+    }
+};
 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     umma::mbar_arrive_expect_tx(bar, bytes);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     umma::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
+                 : "memory");
+}
+
+// Bulk copy without expect_tx (the caller posts the total once).
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      umma::smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
@@ -221,26 +336,32 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     }
 
     const int HG = a.HG, LC = HG * P + 2 * N;
-    const bool conv = a.conv_pool != nullptr;
+    const bool conv = a.conv_pool != nullptr, vec = a.vec != 0;
     const int hs = tid / TH, th = tid - hs * TH, NHS = nthr / TH;
     const int S = a.sps * NHS;  // stages; head hl uses stage hl % S, which belongs to slot hl % NHS
     extern __shared__ __align__(128) unsigned char dec_smem[];
+    const DecodeSmem L(S, TILE_BYTES, ntok, LC, HG, P, a.Wc, sizeof(ActT), conv, vec);
     unsigned char *stages = dec_smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(dec_smem + (size_t)S * TILE_BYTES);
-    const size_t foff = decode_float_offset(S, TILE_BYTES);
-    int *flags = reinterpret_cast<int *>(dec_smem + foff - sizeof(int) * kFlagWords);  // [0, NHS): slot timed out; [NHS]: any
-    float *xs = reinterpret_cast<float *>(dec_smem + foff);  // [ntok][LC] x | B | C after the conv
-    float *uraw = xs + ntok * LC;                      // [ntok][LC] raw inputs (conv only)
-    float *dl = uraw + (conv ? ntok * LC : 0);         // [ntok][HG] Delta
-    float *da = dl + ntok * HG;                        // [ntok][HG] exp(Delta*A)
-    float *ys = da + ntok * HG;                        // [ntok][HG*P] C.h
-    ActT *cs = reinterpret_cast<ActT *>(ys + ntok * HG * P);  // [LC][Wc] old conv state
+    uint64_t *full = reinterpret_cast<uint64_t *>(dec_smem + L.bars);
+    uint64_t *zbar = full + S;  // the z rows (vectorised form)
+    int *flags = reinterpret_cast<int *>(dec_smem + L.flags);  // [0, NHS): slot timed out; [NHS]: any
+    float *xs = reinterpret_cast<float *>(dec_smem + L.xs);
+    float *uraw = reinterpret_cast<float *>(dec_smem + L.uraw);
+    float *dl = reinterpret_cast<float *>(dec_smem + L.dl);
+    float *da = reinterpret_cast<float *>(dec_smem + L.da);
+    float *ys = reinterpret_cast<float *>(dec_smem + L.ys);
+    float *dh = reinterpret_cast<float *>(dec_smem + L.dh);
+    int *scr = reinterpret_cast<int *>(dec_smem + L.scr);
+    ActT *cs = reinterpret_cast<ActT *>(dec_smem + L.cs);
+    ActT *zs = reinterpret_cast<ActT *>(dec_smem + L.zs);
 
     if (tid == 0) {
         for (int st = 0; st < S; ++st) umma::mbar_init(&full[st], 1);
+        umma::mbar_init(zbar, 1);
         umma::fence_mbar_init();
     }
     if (tid < kFlagWords) flags[tid] = 0;
+    if (tid < ntok) scr[tid] = a.scratch ? a.scratch[(int64_t)i * ntok + tid] : -1;
     __syncthreads();
 
     StateT *pool = static_cast<StateT *>(a.ssm_pool);
@@ -251,30 +372,80 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
             if (hl < HG) bulk_load(stages + (size_t)(hl % S) * TILE_BYTES, grp + (int64_t)hl * P * N, TILE_BYTES,
                                    &full[hl % S]);
         }
+    const int HP = a.H * P, GN = a.G * N;
+    const bool zvec = vec && a.z != nullptr;
+    if (zvec && tid == 0) {
+        // the row's z values of the group's heads, one contiguous run per token
+        const uint32_t zb = (uint32_t)(HG * P * sizeof(ActT));
+        umma::mbar_arrive_expect_tx(zbar, zb * (uint32_t)ntok);
+        for (int j = 0; j < ntok; ++j)
+            bulk_copy(zs + (size_t)j * HG * P,
+                      static_cast<const ActT *>(a.z) + ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P, zb, zbar);
+    }
 
     const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * ntok * a.Cd;
-    const int HP = a.H * P, GN = a.G * N;
     ChanRanges cr;
     cr.lo[0] = g * HG * P;    cr.len[0] = HG * P;
     cr.lo[1] = HP + g * N;    cr.len[1] = N;
     cr.lo[2] = HP + GN + g * N; cr.len[2] = N;
     cr.total = LC;
-    if (conv) {
-        conv_phase<ActT>(cr, static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride, a.Wc, a.W,
-                         ntok, u_row, a.Cd, a.conv_w, a.conv_b, cs, uraw, xs);
-    } else {
-        for (int idx = tid; idx < ntok * LC; idx += nthr) {
-            const int j = idx / LC, lc = idx - j * LC;
-            xs[idx] = to_f32(u_row[(int64_t)j * a.Cd + local_to_global(cr, lc)]);
+    // Delta, exp(Delta*A) and D of the group's heads, by threads first, first + stride, ...
+    auto dt_phase = [&](int first, int stride) {
+        for (int idx = first; idx < ntok * HG; idx += stride) {
+            const int j = idx / HG, h = g * HG + (idx - j * HG);
+            const float sdt = load_scalar(a.dt, ((int64_t)i * ntok + j) * a.H + h, a.dt_bf16) +
+                              (a.dt_bias ? a.dt_bias[h] : 0.0f);
+            const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
+            dl[idx] = delta;
+            da[idx] = expf(delta * a.A[h]);
         }
-    }
-    for (int idx = tid; idx < ntok * HG; idx += nthr) {
-        const int j = idx / HG, h = g * HG + (idx - j * HG);
-        const float sdt = load_scalar(a.dt, ((int64_t)i * ntok + j) * a.H + h, a.dt_bf16) +
-                          (a.dt_bias ? a.dt_bias[h] : 0.0f);
-        const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
-        dl[idx] = delta;
-        da[idx] = expf(delta * a.A[h]);
+        for (int hh = first; hh < HG; hh += stride) dh[hh] = a.D ? a.D[g * HG + hh] : 0.0f;
+    };
+    if (vec) {
+        // one thread per 16-byte vector of channels; the threads left over do the per-head work
+        constexpr int VA = Vec16<ActT>::n;
+        const int nv = LC / VA;
+        if (conv) {
+            ActT *cst = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+            for (int v = tid; v < nv; v += nthr) {
+                if constexpr (NT == 1) {
+                    conv_phase_vec<ActT, 4, 1>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA);
+                } else {
+                    switch (ntok) {
+                        case 1: conv_phase_vec<ActT, 4, 1>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
+                        case 2: conv_phase_vec<ActT, 4, 2>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
+                        case 3: conv_phase_vec<ActT, 4, 3>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
+                        default: conv_phase_vec<ActT, 4, 4>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
+                    }
+                }
+            }
+        } else {
+            for (int v = tid; v < ntok * nv; v += nthr) {
+                const int j = v / nv, lc0 = (v - j * nv) * VA;
+                float f[VA];
+                unpack16(*reinterpret_cast<const uint4 *>(u_row + (int64_t)j * a.Cd + local_to_global(cr, lc0)), f);
+                float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)j * LC + lc0);
+#pragma unroll
+                for (int q = 0; q < VA / 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            }
+        }
+        const int busy = conv ? nv : ntok * nv;
+        if (busy < nthr) {
+            if (tid >= busy) dt_phase(tid - busy, nthr - busy);
+        } else {
+            dt_phase(tid, nthr);
+        }
+    } else {
+        if (conv) {
+            conv_phase<ActT>(cr, static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride, a.Wc, a.W,
+                             ntok, u_row, a.Cd, a.conv_w, a.conv_b, cs, uraw, xs);
+        } else {
+            for (int idx = tid; idx < ntok * LC; idx += nthr) {
+                const int j = idx / LC, lc = idx - j * LC;
+                xs[idx] = to_f32(u_row[(int64_t)j * a.Cd + local_to_global(cr, lc)]);
+            }
+        }
+        dt_phase(tid, nthr);
     }
     __syncthreads();
 
@@ -300,7 +471,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
             }
             StateT *dst = grp + (int64_t)hl * P * N;
             if (a.scratch) {
-                const int32_t d = a.scratch[i];
+                const int32_t d = scr[0];
                 dst = d >= 0 ? pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N : nullptr;
             }
 #pragma unroll
@@ -328,6 +499,9 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
             float st[PASSES][VEC];
 #pragma unroll
             for (int pass = 0; pass < PASSES; ++pass) unpack16(tile[pass * TH + th], st[pass]);
+            // the stage is refilled by an asynchronous bulk copy right after the barrier, while the
+            // values just read are first used later: order the reads before that copy
+            umma::fence_async_smem();
             named_sync(1 + hs, TH);
             if (th == 0 && hl + S < HG)
                 bulk_load(stages + (size_t)stg * TILE_BYTES, grp + (int64_t)(hl + S) * P * N, TILE_BYTES, &full[stg]);
@@ -357,7 +531,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
                 ReduceScatter<PASSES, VR / 2>::run(part, lane, idx);
                 if ((lane & (VR / PASSES - 1)) == 0) ys[j * HG * P + hl * P + idx * RP + rsub] = part[0];
                 if (a.scratch) {
-                    const int32_t d = a.scratch[(int64_t)i * ntok + j];
+                    const int32_t d = scr[j];
                     if (d >= 0)
                         store_tile<StateT, P, N>(st, pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N,
                                                  th);
@@ -377,16 +551,52 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         }
     }
     __syncthreads();
-    if (flags[NHS]) return;
+    if (flags[NHS]) {
+        if (zvec && tid == 0) umma::mbar_wait(zbar, 0, kMaxPolls);  // the z copies still in flight (bounded)
+        return;
+    }
 
     // y = C.h + D*x, gated by SiLU(z)
-    const ActT *zr = static_cast<const ActT *>(a.z);
     ActT *yr = static_cast<ActT *>(a.y);
+    if (vec) {
+        constexpr int VA = Vec16<ActT>::n;
+        if (zvec) {
+            if (tid == 0 && !umma::mbar_wait(zbar, 0, kMaxPolls)) {
+                flag_error(a.err, MAMBA_ERR_TIMEOUT);
+                flags[NHS] = 1;
+            }
+            __syncthreads();
+            if (flags[NHS]) return;
+        }
+        const int nvy = HG * P / VA;
+        for (int v = tid; v < ntok * nvy; v += nthr) {
+            const int j = v / nvy, lc0 = (v - j * nvy) * VA;
+            const float Dh = dh[lc0 / P];
+            const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)j * LC + lc0);
+            const float4 *y4 = reinterpret_cast<const float4 *>(ys + (size_t)j * HG * P + lc0);
+            float zf[VA], o[VA];
+            if (zvec) unpack16(*reinterpret_cast<const uint4 *>(zs + (size_t)j * HG * P + lc0), zf);
+#pragma unroll
+            for (int q = 0; q < VA / 4; ++q) {
+                const float4 xv = x4[q], yv = y4[q];
+                o[4 * q] = fmaf(Dh, xv.x, yv.x);
+                o[4 * q + 1] = fmaf(Dh, xv.y, yv.y);
+                o[4 * q + 2] = fmaf(Dh, xv.z, yv.z);
+                o[4 * q + 3] = fmaf(Dh, xv.w, yv.w);
+            }
+            if (zvec) {
+#pragma unroll
+                for (int e = 0; e < VA; ++e) o[e] *= silu_f(zf[e]);
+            }
+            *reinterpret_cast<uint4 *>(yr + ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P + lc0) = pack16(o);
+        }
+        return;
+    }
+    const ActT *zr = static_cast<const ActT *>(a.z);
     for (int idx = tid; idx < ntok * HG * P; idx += nthr) {
         const int j = idx / (HG * P), lc = idx - j * HG * P;
-        const int h = g * HG + lc / P;
         const float xv = xs[j * LC + lc];
-        float yv = ys[idx] + (a.D ? a.D[h] * xv : 0.0f);
+        float yv = fmaf(dh[lc / P], xv, ys[idx]);
         const int64_t o = ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P + lc;
         if (zr) yv *= silu_f(to_f32(zr[o]));
         yr[o] = from_f32<ActT>(yv);
@@ -417,8 +627,6 @@ struct StreamArgs {
     DecodeArgs d;
     int ns;  // tile stages
 };
-
-__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
 // Per-item buffer (byte offsets): xs[LC] | dl[HG] | da[HG] floats, the raw z row (ActT), ys[HG*P]
 // floats; every part 16-byte aligned.
@@ -476,14 +684,6 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, volat
     const bool ok = stream_wait(bar, phase & 1u, abort);
     ++phase;
     return ok;
-}
-
-// Bulk copy without expect_tx (the caller posts the total once).
-__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     umma::smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
-                 : "memory");
 }
 
 template <typename StateT, typename ActT, int P, int N>
@@ -1047,14 +1247,22 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     if (nhs < 1) nhs = 1;
     if (nhs > a.HG) nhs = a.HG;
     if (nhs > 8) nhs = 8;
-    const size_t tile = (size_t)P * N * sizeof(StateT);
-    const size_t rest = sizeof(float) * (size_t)decode_smem_floats(ntok, LC, a.HG, P, conv) +
-                        (conv ? sizeof(ActT) * (size_t)LC * a.Wc : 0);
-    // two stages per head slot (up to 2 * nhs tiles in flight per CTA), fewer if shared memory is short;
-    // several tokens keep each tile in registers for a while, so one stage per slot suffices there and
-    // leaves room for two CTAs per SM
-    int sps = ntok > 1 ? 1 : 2;
-    auto smem_for = [&](int k) { return decode_float_offset(k * nhs, tile) + rest; };
+    const size_t tile = (size_t)P * N * sizeof(StateT), es = sizeof(ActT);
+    // 16-byte vectorised conv and output phases: whole vectors of channels in every range, a
+    // 4-tap conv whose window is exactly W-1+ntok columns, and 16-byte aligned rows
+    constexpr int VA = Vec16<ActT>::n;
+    const size_t HP = (size_t)a.H * P;
+    bool vec = (a.HG * P) % VA == 0 && N % VA == 0 && aligned16(a.xbc) && ((size_t)a.Cd * es) % 16 == 0 &&
+               aligned16(a.y) && (HP * es) % 16 == 0 && (!a.z || aligned16(a.z));
+    if (conv)
+        vec = vec && a.W == 4 && ntok >= 1 && ntok <= 4 && a.Wc == a.W - 1 + ntok && aligned16(a.conv_pool) &&
+              ((size_t)a.conv_stride * es) % 16 == 0 && aligned16(a.conv_w);
+    a.vec = vec ? 1 : 0;
+    auto smem_for = [&](int k) { return DecodeSmem(k * nhs, tile, ntok, LC, a.HG, P, a.Wc, es, conv, vec).total; };
+    // two stages per head slot (up to 2 * nhs tiles in flight per CTA) when two CTAs still fit on an
+    // SM (several tokens keep each tile in registers for a while), else one
+    int sps = 2;
+    if (ntok > 1 && smem_for(2) > 112 * 1024) sps = 1;
     while (sps > 1 && smem_for(sps) > 227 * 1024) --sps;
     const size_t smem = smem_for(sps);
     if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
