@@ -632,7 +632,7 @@ def run_mamba1(torch, args, rank, dist, hbm_peak):
            "hbm_frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "token_layers_per_s": L * batch / (ms * 1e-3),
            "algorithmic_bytes_per_token_layer": M1_BYTES_PER_TOKEN_LAYER, "launches_per_step": 2 * L,
            "launch": "CUDA graph replay (one graph per step)",
-           "state_update": {"kernel": "k_mamba1_update", "us_per_launch": ms_u * 1e3 / L,
+           "state_update": {"kernel": "k_mamba1_stream", "us_per_launch": ms_u * 1e3 / L,
                             "gbs": by_u / (ms_u * 1e-3) / 1e9, "hbm_frac": by_u / (ms_u * 1e-3) / 1e9 / hbm_peak,
                             "algorithmic_bytes_per_launch": batch * M1_UPDATE_BYTES}}
     del ssm, conv

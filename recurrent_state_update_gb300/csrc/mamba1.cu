@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace ms {
 
@@ -145,6 +146,185 @@ __global__ void __launch_bounds__(kM1Threads, N <= 16 ? 3 : 1) k_mamba1_update(c
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// persistent bulk-copy stream (state rows of at most 64 bytes per channel)
+// ---------------------------------------------------------------------------------------
+//
+// Work item = (batch row, block of kM1Threads channels).  A CTA owns one channel block (its
+// channels' rows of A, D and dt_bias stay in registers) and walks the rows rb, rb + kpb, ...
+// One producer thread bulk-copies each item's state rows (kM1Threads x N contiguous values in the
+// slot), x, dt and z slices and the row's B and C into a ring of shared-memory stages, up to NS
+// items ahead; 256 consumer threads (one channel each) update the state from the stage, write it
+// back with evict-first 16-byte stores and write y.  Each stage has a full barrier (the copies'
+// bytes) and an empty barrier (every consumer has used the stage).  All waits are bounded.
+
+constexpr int kM1StreamThreads = kM1Threads + 32;
+constexpr uint32_t kM1Polls = 1u << 24;
+
+__host__ __device__ inline uint32_t m1_al16(uint32_t v) { return (v + 15u) & ~15u; }
+
+// Byte offsets inside one stage.
+struct M1Stage {
+    uint32_t x, dt, z, b, c, hdr, bytes;
+    __host__ __device__ M1Stage(int N, uint32_t es_state, uint32_t es_act) {
+        x = m1_al16(kM1Threads * N * es_state);
+        dt = x + m1_al16(kM1Threads * es_act);
+        z = dt + kM1Threads * 4;
+        b = z + m1_al16(kM1Threads * es_act);
+        c = b + m1_al16(N * es_act);
+        hdr = c + m1_al16(N * es_act);
+        bytes = (hdr + 16 + 127) & ~127u;
+    }
+};
+
+struct M1StreamArgs {
+    M1Args a;
+    int ns, kpb, ncb;
+};
+
+template <typename ActT>
+__device__ __forceinline__ float act_at(const unsigned char *p, int t) {
+    return to_f32(reinterpret_cast<const ActT *>(p)[t]);
+}
+
+template <typename StateT, typename ActT, int N>
+__global__ void __launch_bounds__(kM1StreamThreads, 2) k_mamba1_stream(const M1StreamArgs sa) {
+    const M1Args &a = sa.a;
+    const int NS = sa.ns, kpb = sa.kpb;
+    const int cb = blockIdx.x % sa.ncb, rb = blockIdx.x / sa.ncb;
+    const int tid = threadIdx.x;
+    const int d0 = cb * kM1Threads, nch = min(kM1Threads, a.Dn - d0);
+    const M1Stage L(N, sizeof(StateT), sizeof(ActT));
+    extern __shared__ __align__(128) unsigned char m1_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(m1_smem + (size_t)NS * L.bytes);
+    uint64_t *empty = full + NS;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NS);
+    int *issued = const_cast<int *>(abort_flag) + 1;
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            umma::mbar_init(&full[s], 1);
+            umma::mbar_init(&empty[s], kM1Threads);
+        }
+        umma::fence_mbar_init();
+        *abort_flag = 0;
+        *issued = 0;
+    }
+    __syncthreads();
+
+    if (tid >= kM1Threads) {
+        // ---------------- producer ----------------
+        if (tid == kM1Threads) {
+            const uint32_t es = sizeof(StateT), ea = sizeof(ActT), et = a.dt_bf16 ? 2u : 4u;
+            const uint32_t hb = (uint32_t)nch * N * es, xb = (uint32_t)nch * ea, tb = (uint32_t)nch * et;
+            const uint32_t bcb = (uint32_t)N * ea;
+            int k = 0;
+            for (int i = rb; i < a.batch; i += kpb, ++k) {
+                const int st = k % NS;
+                if (k >= NS) {
+                    bool ok = false;
+                    for (uint32_t it = 0; it < kM1Polls && !ok; ++it) {
+                        ok = umma::mbar_try_wait(&empty[st], (uint32_t)(k / NS - 1) & 1u);
+                        if (!ok && (it & 1023u) == 1023u && *abort_flag) break;
+                    }
+                    if (!ok) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                unsigned char *sp = m1_smem + (size_t)st * L.bytes;
+                int32_t s = a.slot[i];
+                if (s >= a.num_slots) {
+                    if (cb == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+                    s = -1;
+                }
+                *reinterpret_cast<int32_t *>(sp + L.hdr) = s;
+                if (s < 0) {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&full[st])) : "memory");
+                } else {
+                    const int64_t xi = (int64_t)i * a.Dn + d0;
+                    umma::mbar_arrive_expect_tx(&full[st], hb + xb + tb + (a.z ? xb : 0u) + 2 * bcb);
+                    umma::bulk_g2s(sp, static_cast<const StateT *>(a.ssm) + s * a.ssm_stride + (int64_t)d0 * N, hb,
+                                   &full[st]);
+                    umma::bulk_g2s(sp + L.x, static_cast<const ActT *>(a.x) + xi, xb, &full[st]);
+                    umma::bulk_g2s(sp + L.dt, static_cast<const unsigned char *>(a.dt) + xi * et, tb, &full[st]);
+                    if (a.z) umma::bulk_g2s(sp + L.z, static_cast<const ActT *>(a.z) + xi, xb, &full[st]);
+                    umma::bulk_g2s(sp + L.b, static_cast<const ActT *>(a.B) + (int64_t)i * N, bcb, &full[st]);
+                    umma::bulk_g2s(sp + L.c, static_cast<const ActT *>(a.C) + (int64_t)i * N, bcb, &full[st]);
+                }
+                *issued = k + 1;
+            }
+        }
+    } else {
+        // ---------------- consumers (thread = channel d0 + tid) ----------------
+        const int d = d0 + tid;
+        const bool live = tid < nch;
+        float Ar[N];
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 v = live ? reinterpret_cast<const float4 *>(a.A + (int64_t)d * N)[q] : make_float4(0, 0, 0, 0);
+            Ar[4 * q] = v.x * kLog2e;
+            Ar[4 * q + 1] = v.y * kLog2e;
+            Ar[4 * q + 2] = v.z * kLog2e;
+            Ar[4 * q + 3] = v.w * kLog2e;
+        }
+        const float Dd = (live && a.D) ? a.D[d] : 0.0f, bias = (live && a.dt_bias) ? a.dt_bias[d] : 0.0f;
+        int k = 0;
+        for (int i = rb; i < a.batch; i += kpb, ++k) {
+            const int st = k % NS;
+            bool ok = false;
+            for (uint32_t it = 0; it < kM1Polls && !ok; ++it) {
+                ok = umma::mbar_try_wait(&full[st], (uint32_t)(k / NS) & 1u);
+                if (!ok && (it & 1023u) == 1023u && *abort_flag) break;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            const unsigned char *sp = m1_smem + (size_t)st * L.bytes;
+            const int32_t s = *reinterpret_cast<const int32_t *>(sp + L.hdr);
+            if (s >= 0 && live) {
+                float h[N];
+                load_row<StateT, N>(reinterpret_cast<const StateT *>(sp) + (size_t)tid * N, h);
+                const float xv = act_at<ActT>(sp + L.x, tid);
+                const float sdt = (a.dt_bf16 ? to_f32(reinterpret_cast<const bf16 *>(sp + L.dt)[tid])
+                                             : reinterpret_cast<const float *>(sp + L.dt)[tid]) + bias;
+                const float zv = a.z ? act_at<ActT>(sp + L.z, tid) : 0.0f;
+                float bv[N], cv[N];
+                load_row<ActT, N>(reinterpret_cast<const ActT *>(sp + L.b), bv);
+                load_row<ActT, N>(reinterpret_cast<const ActT *>(sp + L.c), cv);
+                const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
+                const float dx = delta * xv;
+                float acc = 0.0f;
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    h[n] = fmaf(ex2_approx(delta * Ar[n]), h[n], dx * bv[n]);
+                    acc = fmaf(cv[n], h[n], acc);
+                }
+                StateT *dst = static_cast<StateT *>(a.ssm) + s * a.ssm_stride + (int64_t)d * N;
+                constexpr int V = Vec16<StateT>::n;
+#pragma unroll
+                for (int q = 0; q < N / V; ++q) {
+                    float f[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) f[e] = h[q * V + e];
+                    __stcs(reinterpret_cast<uint4 *>(dst) + q, pack16(f));
+                }
+                float yv = acc + Dd * xv;
+                if (a.z) yv *= silu_f(zv);
+                static_cast<ActT *>(a.y)[(int64_t)i * a.Dn + d] = from_f32<ActT>(yv);
+            }
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&empty[st])) : "memory");
+        }
+    }
+    __syncthreads();
+    if (tid == kM1Threads && *abort_flag) {
+        // a wait gave up: report it and let the copies still in flight land (bounded)
+        flag_error(a.err, MAMBA_ERR_TIMEOUT);
+        const int n = *issued;
+        for (int k = n > NS ? n - NS : 0; k < n; ++k) umma::mbar_wait(&full[k % NS], (uint32_t)(k / NS) & 1u, kM1Polls);
+    }
+}
+
 int sm_count_m1() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -152,8 +332,39 @@ int sm_count_m1() {
     return n;
 }
 
+// The stream kernel when a channel's state row is at most 64 bytes and every slice it copies is
+// 16-byte aligned; false when the strided kernel must run instead.
+template <typename StateT, typename ActT, int N>
+bool launch_m1_stream(const M1Args &a, int batch, cudaStream_t st) {
+    constexpr size_t es = sizeof(StateT), ea = sizeof(ActT);
+    if constexpr (N * es > 64) {
+        return false;
+    } else {
+    const size_t et = a.dt_bf16 ? 2 : 4;
+    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(a.ssm) || !al(a.x) || !al(a.dt) || (a.z && !al(a.z)) || !al(a.B) || !al(a.C) ||
+        ((size_t)a.Dn * ea) % 16 || ((size_t)a.Dn * et) % 16 || ((size_t)N * ea) % 16 || ((size_t)a.ssm_stride * es) % 16)
+        return false;
+    const M1Stage L(N, (uint32_t)es, (uint32_t)ea);
+    const size_t tail = 16 * 8 * 2 + 16;  // barriers of up to 16 stages + flags
+    int ns = 16;
+    while (ns > 2 && (size_t)ns * L.bytes + tail > 110 * 1024) --ns;
+    const size_t smem = (size_t)ns * L.bytes + (size_t)ns * 16 + 16;
+    const int sms = std::max(1, sm_count_m1());
+    const int ncb = (a.Dn + kM1Threads - 1) / kM1Threads;
+    const int kpb = std::min(batch, std::max(1, 2 * sms / ncb));
+    auto kern = k_mamba1_stream<StateT, ActT, N>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+    M1StreamArgs sa;
+    sa.a = a; sa.ns = ns; sa.kpb = kpb; sa.ncb = ncb;
+    kern<<<ncb * kpb, kM1StreamThreads, smem, st>>>(sa);
+    return true;
+    }
+}
+
 template <typename StateT, typename ActT, int N>
 void launch_m1n(const M1Args &a, int batch, cudaStream_t st) {
+    if (launch_m1_stream<StateT, ActT, N>(a, batch, st)) return;
     // one wave: the blocks resident at once, split over the channel blocks; rows strided over the rest
     const int cb = (a.Dn + kM1Threads - 1) / kM1Threads;
     int occ = 1;
