@@ -160,16 +160,40 @@ __device__ __forceinline__ void set_word(uint4 &q, int c, uint32_t w) {
     else q.w = w;
 }
 
+// The new window of V channels after NTK tokens: the last WC entries of [old window (WC) | tokens],
+// per channel, assembled from the raw values.
+template <typename ActT, int NTK, int WC>
+__device__ __forceinline__ void conv_new_window(const uint4 (&win)[WC], const uint4 (&tok)[NTK], uint4 (&nw)[WC]) {
+    constexpr int V = Vec16<ActT>::n, PW = (int)(4 / sizeof(ActT));
+    auto input = [&](int v, int m) -> uint32_t {
+        return m < WC ? raw_at<PW>(win, v * WC + m) : raw_at<PW>(tok, (m - WC) * V + v);
+    };
+#pragma unroll
+    for (int wi = 0; wi < WC * 4; ++wi) {  // 32-bit words of the new window
+        uint32_t word;
+        if (PW == 1) {
+            const int e = wi, v = e / WC, k = e - v * WC;
+            word = input(v, NTK + k);
+        } else {
+            const int e0 = 2 * wi, e1 = e0 + 1;
+            const int v0 = e0 / WC, k0 = e0 - v0 * WC, v1 = e1 / WC, k1 = e1 - v1 * WC;
+            word = input(v0, NTK + k0) | (input(v1, NTK + k1) << 16);
+        }
+        set_word(nw[wi / 4], wi % 4, word);
+    }
+}
+
 // Conv phase of one 16-byte vector of channels (V channels, local channels lc0 .. lc0 + V - 1) for
-// NTK tokens with a W-tap kernel and a window of exactly W-1+NTK columns: the vector's window is
-// W-1+NTK contiguous 16-byte loads (a slot keeps each channel's columns together), every load is
-// issued before any arithmetic, and the new window (the last W-1+NTK entries of [old window |
-// tokens]) is assembled from the raw values, so the conv state stays bit-exact.
-template <typename ActT, int W, int NTK>
+// NTK tokens with a W-tap kernel and a window of WC >= W-1 columns: the vector's window is WC
+// contiguous 16-byte loads (a slot keeps each channel's columns together), every load is issued
+// before any arithmetic, and the new window is assembled from the raw values, so the conv state
+// stays bit-exact.  With write_window false the new window is left for conv_window_shift.
+template <typename ActT, int W, int NTK, int WC>
 __device__ __forceinline__ void conv_phase_vec(const ChanRanges &cr, ActT *cstate, const ActT *u_row, int Cd,
                                                const float *__restrict__ w, const float *__restrict__ b,
-                                               float *xs, int lc0) {
-    constexpr int V = Vec16<ActT>::n, PW = (int)(4 / sizeof(ActT)), WC = W - 1 + NTK;
+                                               float *xs, int lc0, bool write_window) {
+    static_assert(WC >= W - 1, "the window holds at least the W-1 inputs before a token");
+    constexpr int V = Vec16<ActT>::n, PW = (int)(4 / sizeof(ActT));
     const int LC = cr.total;
     const int c0 = local_to_global(cr, lc0);
     uint4 *sp = reinterpret_cast<uint4 *>(cstate + (int64_t)c0 * WC);
@@ -208,22 +232,76 @@ __device__ __forceinline__ void conv_phase_vec(const ChanRanges &cr, ActT *cstat
 #pragma unroll
         for (int q = 0; q < V / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
     }
-    uint4 nw[WC];
+    if (write_window) {
+        uint4 nw[WC];
+        conv_new_window<ActT, NTK, WC>(win, tok, nw);
 #pragma unroll
-    for (int wi = 0; wi < WC * 4; ++wi) {  // 32-bit words of the new window
-        uint32_t word;
-        if (PW == 1) {
-            const int e = wi, v = e / WC, k = e - v * WC;
-            word = input(v, NTK + k);
-        } else {
-            const int e0 = 2 * wi, e1 = e0 + 1;
-            const int v0 = e0 / WC, k0 = e0 - v0 * WC, v1 = e1 / WC, k1 = e1 - v1 * WC;
-            word = input(v0, NTK + k0) | (input(v1, NTK + k1) << 16);
-        }
-        set_word(nw[wi / 4], wi % 4, word);
+        for (int k = 0; k < WC; ++k) sp[k] = nw[k];
     }
+}
+
+// The window update of one channel vector whose conv_phase_vec left it unwritten: the old window
+// is read again (no other CTA writes it) and shifted by the tokens.
+template <typename ActT, int NTK, int WC>
+__device__ __forceinline__ void conv_window_shift(const ChanRanges &cr, ActT *cstate, const ActT *u_row, int Cd,
+                                                  int lc0) {
+    const int c0 = local_to_global(cr, lc0);
+    uint4 *sp = reinterpret_cast<uint4 *>(cstate + (int64_t)c0 * WC);
+    uint4 win[WC], tok[NTK], nw[WC];
+#pragma unroll
+    for (int k = 0; k < WC; ++k) win[k] = sp[k];
+#pragma unroll
+    for (int j = 0; j < NTK; ++j) tok[j] = *reinterpret_cast<const uint4 *>(u_row + (int64_t)j * Cd + c0);
+    conv_new_window<ActT, NTK, WC>(win, tok, nw);
 #pragma unroll
     for (int k = 0; k < WC; ++k) sp[k] = nw[k];
+}
+
+// The compiled vectorised conv forms: a 4-tap kernel, 1..4 tokens, a window of W-1 columns or of
+// W-1+ntok (speculative columns).
+template <typename ActT, int NTK>
+__device__ __forceinline__ void conv_vec_wc(bool wc_min, const ChanRanges &cr, ActT *cst, const ActT *u_row, int Cd,
+                                            const float *w, const float *b, float *xs, int lc0, bool wr) {
+    if (wc_min) conv_phase_vec<ActT, 4, NTK, 3>(cr, cst, u_row, Cd, w, b, xs, lc0, wr);
+    else conv_phase_vec<ActT, 4, NTK, 3 + NTK>(cr, cst, u_row, Cd, w, b, xs, lc0, wr);
+}
+template <typename ActT, int NT>
+__device__ __forceinline__ void conv_vec(int ntok, bool wc_min, const ChanRanges &cr, ActT *cst, const ActT *u_row,
+                                         int Cd, const float *w, const float *b, float *xs, int lc0, bool wr) {
+    if constexpr (NT == 1) {
+        conv_vec_wc<ActT, 1>(wc_min, cr, cst, u_row, Cd, w, b, xs, lc0, wr);
+    } else {
+        switch (ntok) {
+            case 1: conv_vec_wc<ActT, 1>(wc_min, cr, cst, u_row, Cd, w, b, xs, lc0, wr); break;
+            case 2: conv_vec_wc<ActT, 2>(wc_min, cr, cst, u_row, Cd, w, b, xs, lc0, wr); break;
+            case 3: conv_vec_wc<ActT, 3>(wc_min, cr, cst, u_row, Cd, w, b, xs, lc0, wr); break;
+            default: conv_vec_wc<ActT, 4>(wc_min, cr, cst, u_row, Cd, w, b, xs, lc0, wr); break;
+        }
+    }
+}
+template <typename ActT, int NTK>
+__device__ __forceinline__ void shift_wc(bool wc_min, const ChanRanges &cr, ActT *cst, const ActT *u_row, int Cd, int lc0) {
+    if (wc_min) conv_window_shift<ActT, NTK, 3>(cr, cst, u_row, Cd, lc0);
+    else conv_window_shift<ActT, NTK, 3 + NTK>(cr, cst, u_row, Cd, lc0);
+}
+template <typename ActT, int NT>
+__device__ __forceinline__ void shift_vec(int ntok, bool wc_min, const ChanRanges &cr, ActT *cst, const ActT *u_row,
+                                          int Cd, int lc0) {
+    if constexpr (NT == 1) {
+        shift_wc<ActT, 1>(wc_min, cr, cst, u_row, Cd, lc0);
+    } else {
+        switch (ntok) {
+            case 1: shift_wc<ActT, 1>(wc_min, cr, cst, u_row, Cd, lc0); break;
+            case 2: shift_wc<ActT, 2>(wc_min, cr, cst, u_row, Cd, lc0); break;
+            case 3: shift_wc<ActT, 3>(wc_min, cr, cst, u_row, Cd, lc0); break;
+            default: shift_wc<ActT, 4>(wc_min, cr, cst, u_row, Cd, lc0); break;
+        }
+    }
+}
+
+// All threads of all CTAs of the cluster (hardware barrier; the CTAs of a cluster are co-resident).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------
@@ -249,6 +327,7 @@ struct DecodeArgs {
     int H, G, HG, W, Wc, Cd;
     int sps;  // state-tile stages per head slot
     int vec;  // 16-byte vectorised conv / output phases (see DecodeSmem)
+    int ksplit;  // CTAs (one cluster) per (row, group), each taking HG / ksplit heads
 };
 
 // Bound on the polls of one mbarrier wait (a copy that never lands is reported, not waited on forever).
@@ -318,7 +397,9 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     using TL = Tile<StateT, P, N>;
     constexpr int VEC = TL::VEC, VR = TL::VR, TH = TL::TH, RP = TL::RP, PASSES = TL::PASSES;
     constexpr uint32_t TILE_BYTES = (uint32_t)(P * N * sizeof(StateT));
-    const int g = blockIdx.x, i = blockIdx.y;
+    // blockIdx.x = group * ksplit + rank: the ksplit CTAs of a (row, group) form one cluster and
+    // split the group's heads
+    const int ksplit = a.ksplit, g = blockIdx.x / ksplit, rank = blockIdx.x - g * ksplit, i = blockIdx.y;
     const int ntok = NT > 0 ? NT : a.ntok;
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
 
@@ -335,7 +416,8 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         return;
     }
 
-    const int HG = a.HG, LC = HG * P + 2 * N;
+    const int HG = a.HG / ksplit, LC = HG * P + 2 * N;  // this CTA's heads and local channels
+    const int hg0 = g * a.HG + rank * HG;                // global index of its first head
     const bool conv = a.conv_pool != nullptr, vec = a.vec != 0;
     const int hs = tid / TH, th = tid - hs * TH, NHS = nthr / TH;
     const int S = a.sps * NHS;  // stages; head hl uses stage hl % S, which belongs to slot hl % NHS
@@ -365,7 +447,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     __syncthreads();
 
     StateT *pool = static_cast<StateT *>(a.ssm_pool);
-    StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)g * HG * P * N;
+    StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)hg0 * P * N;
     if (th == 0)
         for (int k = 0; k < a.sps; ++k) {
             const int hl = hs + k * NHS;
@@ -380,26 +462,26 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         umma::mbar_arrive_expect_tx(zbar, zb * (uint32_t)ntok);
         for (int j = 0; j < ntok; ++j)
             bulk_copy(zs + (size_t)j * HG * P,
-                      static_cast<const ActT *>(a.z) + ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P, zb, zbar);
+                      static_cast<const ActT *>(a.z) + ((int64_t)i * ntok + j) * HP + (int64_t)hg0 * P, zb, zbar);
     }
 
     const ActT *u_row = static_cast<const ActT *>(a.xbc) + (int64_t)i * ntok * a.Cd;
     ChanRanges cr;
-    cr.lo[0] = g * HG * P;    cr.len[0] = HG * P;
+    cr.lo[0] = hg0 * P;       cr.len[0] = HG * P;
     cr.lo[1] = HP + g * N;    cr.len[1] = N;
     cr.lo[2] = HP + GN + g * N; cr.len[2] = N;
     cr.total = LC;
     // Delta, exp(Delta*A) and D of the group's heads, by threads first, first + stride, ...
     auto dt_phase = [&](int first, int stride) {
         for (int idx = first; idx < ntok * HG; idx += stride) {
-            const int j = idx / HG, h = g * HG + (idx - j * HG);
+            const int j = idx / HG, h = hg0 + (idx - j * HG);
             const float sdt = load_scalar(a.dt, ((int64_t)i * ntok + j) * a.H + h, a.dt_bf16) +
                               (a.dt_bias ? a.dt_bias[h] : 0.0f);
             const float delta = a.dt_softplus ? softplus_f(sdt) : sdt;
             dl[idx] = delta;
             da[idx] = expf(delta * a.A[h]);
         }
-        for (int hh = first; hh < HG; hh += stride) dh[hh] = a.D ? a.D[g * HG + hh] : 0.0f;
+        for (int hh = first; hh < HG; hh += stride) dh[hh] = a.D ? a.D[hg0 + hh] : 0.0f;
     };
     if (vec) {
         // one thread per 16-byte vector of channels; the threads left over do the per-head work
@@ -407,17 +489,11 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         const int nv = LC / VA;
         if (conv) {
             ActT *cst = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+            // split: the group's B and C windows are read by every CTA of the cluster and written by
+            // its first CTA after the cluster barrier below
             for (int v = tid; v < nv; v += nthr) {
-                if constexpr (NT == 1) {
-                    conv_phase_vec<ActT, 4, 1>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA);
-                } else {
-                    switch (ntok) {
-                        case 1: conv_phase_vec<ActT, 4, 1>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
-                        case 2: conv_phase_vec<ActT, 4, 2>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
-                        case 3: conv_phase_vec<ActT, 4, 3>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
-                        default: conv_phase_vec<ActT, 4, 4>(cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA); break;
-                    }
-                }
+                const bool wr = ksplit == 1 || v * VA < HG * P;
+                conv_vec<ActT, NT>(ntok, a.Wc == 3, cr, cst, u_row, a.Cd, a.conv_w, a.conv_b, xs, v * VA, wr);
             }
         } else {
             for (int v = tid; v < ntok * nv; v += nthr) {
@@ -447,6 +523,15 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         }
         dt_phase(tid, nthr);
     }
+    if (ksplit > 1) {
+        cluster_sync();  // every CTA of the cluster has read the old B and C windows
+        if (conv && rank == 0) {
+            constexpr int VA = Vec16<ActT>::n;
+            ActT *cst = static_cast<ActT *>(a.conv_pool) + (int64_t)s * a.conv_stride;
+            for (int v = HG * P / VA + tid; v < LC / VA; v += nthr)
+                shift_vec<ActT, NT>(ntok, a.Wc == 3, cr, cst, u_row, a.Cd, v * VA);
+        }
+    }
     __syncthreads();
 
     const int rsub = th / VR, n0 = (th - rsub * VR) * VEC;
@@ -472,7 +557,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
             StateT *dst = grp + (int64_t)hl * P * N;
             if (a.scratch) {
                 const int32_t d = scr[0];
-                dst = d >= 0 ? pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N : nullptr;
+                dst = d >= 0 ? pool + (int64_t)d * a.ssm_stride + (int64_t)(hg0 + hl) * P * N : nullptr;
             }
 #pragma unroll
             for (int pass = 0; pass < PASSES; ++pass) {
@@ -533,7 +618,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
                 if (a.scratch) {
                     const int32_t d = scr[j];
                     if (d >= 0)
-                        store_tile<StateT, P, N>(st, pool + (int64_t)d * a.ssm_stride + (int64_t)(g * HG + hl) * P * N,
+                        store_tile<StateT, P, N>(st, pool + (int64_t)d * a.ssm_stride + (int64_t)(hg0 + hl) * P * N,
                                                  th);
                 }
             }
@@ -588,7 +673,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
 #pragma unroll
                 for (int e = 0; e < VA; ++e) o[e] *= silu_f(zf[e]);
             }
-            *reinterpret_cast<uint4 *>(yr + ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P + lc0) = pack16(o);
+            *reinterpret_cast<uint4 *>(yr + ((int64_t)i * ntok + j) * HP + (int64_t)hg0 * P + lc0) = pack16(o);
         }
         return;
     }
@@ -597,7 +682,7 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
         const int j = idx / (HG * P), lc = idx - j * HG * P;
         const float xv = xs[j * LC + lc];
         float yv = fmaf(dh[lc / P], xv, ys[idx]);
-        const int64_t o = ((int64_t)i * ntok + j) * HP + (int64_t)g * HG * P + lc;
+        const int64_t o = ((int64_t)i * ntok + j) * HP + (int64_t)hg0 * P + lc;
         if (zr) yv *= silu_f(to_f32(zr[o]));
         yr[o] = from_f32<ActT>(yv);
     }
@@ -1237,28 +1322,50 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     return launch_status();
 }
 
+static int device_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    }
+    return n;
+}
+
 template <typename StateT, typename ActT, int P, int N>
 static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, cudaStream_t stream) {
     using TL = Tile<StateT, P, N>;
     DecodeArgs a = a0;
-    const int LC = a.HG * P + 2 * N;
     const bool conv = a.conv_pool != nullptr;
-    int nhs = 256 / TL::TH;
-    if (nhs < 1) nhs = 1;
-    if (nhs > a.HG) nhs = a.HG;
-    if (nhs > 8) nhs = 8;
     const size_t tile = (size_t)P * N * sizeof(StateT), es = sizeof(ActT);
     // 16-byte vectorised conv and output phases: whole vectors of channels in every range, a
-    // 4-tap conv whose window is exactly W-1+ntok columns, and 16-byte aligned rows
+    // 4-tap conv whose window is W-1 or W-1+ntok columns, and 16-byte aligned rows
     constexpr int VA = Vec16<ActT>::n;
     const size_t HP = (size_t)a.H * P;
     bool vec = (a.HG * P) % VA == 0 && N % VA == 0 && aligned16(a.xbc) && ((size_t)a.Cd * es) % 16 == 0 &&
                aligned16(a.y) && (HP * es) % 16 == 0 && (!a.z || aligned16(a.z));
     if (conv)
-        vec = vec && a.W == 4 && ntok >= 1 && ntok <= 4 && a.Wc == a.W - 1 + ntok && aligned16(a.conv_pool) &&
+        vec = vec && a.W == 4 && ntok >= 1 && ntok <= 4 && (a.Wc == a.W - 1 || a.Wc == a.W - 1 + ntok) &&
+              aligned16(a.conv_pool) &&
               ((size_t)a.conv_stride * es) % 16 == 0 && aligned16(a.conv_w);
     a.vec = vec ? 1 : 0;
-    auto smem_for = [&](int k) { return DecodeSmem(k * nhs, tile, ntok, LC, a.HG, P, a.Wc, es, conv, vec).total; };
+    // Small single-token batches: batch x groups CTAs would leave most SMs idle, so the heads of a
+    // group are split over a cluster of up to 8 CTAs (a power of two dividing the heads per group,
+    // at most enough for two CTAs per SM).
+    int ksplit = 1;
+    const int sms = device_sms();
+    if (vec && ntok == 1 && sms > 0 && (int64_t)a.batch * a.G < 2 * sms) {
+        const int64_t want = (2 * (int64_t)sms + (int64_t)a.batch * a.G - 1) / ((int64_t)a.batch * a.G);
+        while (ksplit * 2 <= 8 && ksplit * 2 <= want && a.HG % (ksplit * 2) == 0 && ((a.HG / (ksplit * 2)) * P) % VA == 0)
+            ksplit *= 2;
+    }
+    for (;; ksplit = 1) {
+    const int HGL = a.HG / ksplit, LC = HGL * P + 2 * N;
+    int nhs = 256 / TL::TH;
+    if (nhs < 1) nhs = 1;
+    if (nhs > HGL) nhs = HGL;
+    if (nhs > 8) nhs = 8;
+    auto smem_for = [&](int k) { return DecodeSmem(k * nhs, tile, ntok, LC, HGL, P, a.Wc, es, conv, vec).total; };
     // two stages per head slot (up to 2 * nhs tiles in flight per CTA) when two CTAs still fit on an
     // SM (several tokens keep each tile in registers for a while), else one
     int sps = 2;
@@ -1267,20 +1374,40 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     const size_t smem = smem_for(sps);
     if (smem > 227 * 1024) return MAMBA_EUNSUPPORTED;
     a.sps = sps;
+    a.ksplit = ksplit;
     if constexpr (TL::TH <= kStreamConsumers && kStreamConsumers % TL::TH == 0) {
-        if (ntok == 1 && a.scratch == nullptr) {
+        if (ntok == 1 && a.scratch == nullptr && ksplit == 1) {
             const int rc = launch_stream<StateT, ActT, P, N>(a, stream);
             if (rc != 1) return rc;
         }
     }
-    const dim3 grid(a.G, a.batch), block(nhs * TL::TH);
     auto kern = ntok == 1 ? k_decode<StateT, ActT, P, N, 1> : k_decode<StateT, ActT, P, N, 0>;
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return MAMBA_ECUDA;
     }
-    kern<<<grid, block, smem, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.G * ksplit, a.batch);
+    cfg.blockDim = dim3(nhs * TL::TH);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (ksplit > 1) {
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            continue;  // no room for such a cluster: one CTA per (row, group)
+        }
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
+    }
 }
 
 // The compiled (head_dim, d_state) tiles.
