@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
                         float v0 = yd[qq] + ei * yo[qq] + Dh * __uint_as_float(xw[e] << 16);
                         float v1 = yd[qq + 1] + ei * yo[qq + 1] + Dh * __uint_as_float(xw[e] & 0xffff0000u);
                         if (gate) {
-                            v0 *= silu_f(__uint_as_float(zw[e] << 16));
-                            v1 *= silu_f(__uint_as_float(zw[e] & 0xffff0000u));
+                            v0 *= silu_fast(__uint_as_float(zw[e] << 16));
+                            v1 *= silu_fast(__uint_as_float(zw[e] & 0xffff0000u));
                         }
                         ow[e] = pack_bf16x2(v0, v1);
                     }

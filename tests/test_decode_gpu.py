@@ -301,6 +301,33 @@ def test_speculative_decode_and_commit():
     np.testing.assert_array_equal(f64(conv), e_conv)
 
 
+@pytest.mark.parametrize("batch,spec", [(3, 1), (200, 1), (5, 0)])
+def test_single_token_into_scratch_slots(batch, spec):
+    """One token whose state goes to a scratch slot (main slot untouched): small batches take the
+    head split over a cluster, large ones one CTA per (row, group); conv windows of W-1 and W
+    columns."""
+    import torch
+    S, seed = 2 * batch + 16, 80 + batch
+    shape, ssm, conv = _nemotron_pools(S, seed, spec=spec)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    ids = wl.rng(seed, 3).choice(S, size=2 * batch, replace=False).astype(np.int32)
+    slot, scratch = ids[:batch], ids[batch:].reshape(batch, 1)
+    o_ssm, o_conv = f64(ssm), f64(conv)
+    ssm0 = ssm.clone()
+    dev, o = _step_inputs(layer, seed, 0, batch, ntok=1)
+    y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, scratch_t=to_i32(scratch))
+    torch.cuda.synchronize()
+    y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
+    sl = torch.from_numpy(slot).long().cuda()
+    assert torch.equal(ssm[sl], ssm0[sl])
+    sj = torch.from_numpy(scratch[:, 0].copy()).long().cuda()
+    assert tile_rel_err(f64(ssm[sj]), o_ssm[scratch[:, 0]], 2) < BF16_STEP_TOL
+    assert tile_rel_err(f64(y).reshape(batch, shape.nheads, -1), y_o.reshape(batch, shape.nheads, -1), 1) < 2e-2
+    np.testing.assert_array_equal(f64(conv[sl]), o_conv[slot])
+
+
 def test_device_side_errors_leave_rows_untouched():
     import torch
     S, batch, seed = 16, 4, 70
