@@ -12,11 +12,12 @@
 // all in fp32 (the nearest code on the grid of step s).
 //
 // Design (GB300): all three are HBM streaming passes.  The copy moves 16-byte vectors, 16 KB
-// per block, over the concatenation of a slot's SSM and conv bytes.  Store and load run one
-// thread per (head, 8 adjacent d_state columns) for the store, which stages four heads' tiles in
-// shared memory with one bulk async copy so each column's maximum is found by one thread, and
-// per (head, 8 columns, share of the rows) for the load; 16-byte accesses, every row read or
-// written as one contiguous run.
+// per block, over the concatenation of a slot's SSM and conv bytes.  The store runs one warp
+// per (row, head): the head's tile arrives in shared memory with one bulk async copy, and a
+// thread per (8 adjacent d_state columns, half of the rows) finds the column maxima, combined
+// with a shuffle; the load runs 128 threads per (row, head), one per (8 columns, share of the
+// rows), each issuing all of its rows' code loads before converting any; 16-byte accesses,
+// every row read or written as one contiguous run.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -26,8 +27,9 @@ namespace {
 
 constexpr int kCopyThreads = 256;
 constexpr int kCopyBytes = kCopyThreads * 16 * 4;  // bytes one copy block moves
-constexpr int kQThreads = 256;
-constexpr int kStoreHeads = 4;           // heads quantised by one store block
+constexpr int kQThreads = 128;
+constexpr int kStoreHeads = 1;           // heads quantised by one store block (more blocks in flight)
+constexpr int kLoadRows = 8;             // rows per thread and pass of the load
 constexpr uint32_t kQPolls = 1u << 24;  // bound on the wait for a staged tile
 
 inline size_t align256(size_t b) { return (b + 255) / 256 * 256; }
@@ -254,16 +256,27 @@ __global__ void __launch_bounds__(kQThreads) k_ckpt_load_int8(const QArgs a) {
     const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
     const int8_t *q = reinterpret_cast<const int8_t *>(entry + a.lay.q) + (int64_t)h * a.P * a.N + 8 * co;
     StateT *dst = reinterpret_cast<StateT *>(a.ssm + sl * a.ssm_stride) + (int64_t)h * a.P * a.N + 8 * co;
-    for (int p = rs; p < a.P; p += shares) {
-        const uint2 c = *reinterpret_cast<const uint2 *>(q + (int64_t)p * a.N);
-        float v[8];
+    // kLoadRows rows per pass, their codes loaded before any is converted
+    for (int p0 = rs; p0 < a.P; p0 += shares * kLoadRows) {
+        uint2 c[kLoadRows];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t word = k < 4 ? c.x : c.y;
-            const int code = (int)(int8_t)((word >> (8 * (k & 3))) & 0xffu);
-            v[k] = (float)code * sc[k];
+        for (int r = 0; r < kLoadRows; ++r) {
+            const int p = p0 + r * shares;
+            c[r] = p < a.P ? *reinterpret_cast<const uint2 *>(q + (int64_t)p * a.N) : make_uint2(0u, 0u);
         }
-        store8(dst + (int64_t)p * a.N, v);
+#pragma unroll
+        for (int r = 0; r < kLoadRows; ++r) {
+            const int p = p0 + r * shares;
+            if (p >= a.P) break;
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t word = k < 4 ? c[r].x : c[r].y;
+                const int code = (int)(int8_t)((word >> (8 * (k & 3))) & 0xffu);
+                v[k] = (float)code * sc[k];
+            }
+            store8(dst + (int64_t)p * a.N, v);
+        }
     }
 }
 
@@ -380,7 +393,7 @@ extern "C" int mamba_ckpt_load_int8(const mamba_layer_desc *d, void *ssm_pool, i
     const int rc = q_args(d, ssm_pool, ssm_slot_stride, conv_pool, conv_slot_stride, num_slots, dst_slots, src_entries,
                           n, store, num_entries, err_word, a);
     if (rc != MAMBA_OK || n == 0) return rc;
-    const int conv_blocks = conv_pool ? (int)((a.conv_bytes + kCopyBytes - 1) / kCopyBytes) : 0;
+    const int conv_blocks = conv_pool ? (int)((a.conv_bytes + 64 * kQThreads - 1) / (64 * kQThreads)) : 0;
     const dim3 grid(a.H + conv_blocks, n);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d->state_dtype == MAMBA_BF16) k_ckpt_load_int8<bf16><<<grid, kQThreads, 0, st>>>(a);
