@@ -1083,7 +1083,7 @@ struct ConvArgs {
 // channel's W-1 columns contiguous, so the vector's window is W-1 contiguous 16-byte loads.  All
 // rows' loads are issued before any arithmetic; the new windows (shifted by one, the token
 // appended) and the outputs are written back as 16-byte stores.
-constexpr int kConvRows = 2;
+constexpr int kConvRows = 4;
 constexpr int kConvThreads = 128;
 
 template <typename ActT, int W>
