@@ -165,6 +165,24 @@ __global__ void __launch_bounds__(BulkGeom<W>::THREADS, BulkGeom<W>::MINB) k_con
         for (int k = 0; k < W; ++k) wt[v][k] = has_vec ? a.w[(int64_t)(c0 + v) * W + k] : 0.0f;
         bv[v] = has_vec && a.b ? a.b[c0 + v] : 0.0f;
     }
+    // the sequence holding this thread's current token and what its window seed needs, kept in
+    // registers across tiles (a thread's tokens only increase): advanced only at a boundary
+    int s = -1, s_begin = 0, s_end = 0;
+    bool live = true;
+    const ActT *sp = nullptr;
+    auto enter = [&](int t) {
+        if (s < 0) {
+            s = seq_of(a.cu, a.nseq, t);
+        } else {
+            while (a.cu[s + 1] <= t) ++s;  // empty sequences are skipped
+        }
+        s_begin = a.cu[s];
+        s_end = a.cu[s + 1];
+        const int32_t sl = a.slot ? a.slot[s] : -1;
+        live = sl >= -1 && sl < a.num_slots;
+        const bool has = a.conv_pool && sl >= 0 && live && a.init && a.init[s];
+        sp = has ? static_cast<const ActT *>(a.conv_pool) + sl * a.conv_stride + (int64_t)c0 * a.Wc : nullptr;
+    };
     bool failed = false;
     int i = 0;
     for (int tb = tb0; tb < ntb; tb += tb_step, ++i) {
@@ -175,34 +193,25 @@ __global__ void __launch_bounds__(BulkGeom<W>::THREADS, BulkGeom<W>::MINB) k_con
             if (tb + (S - 1) * tb_step < ntb) issue(tb + (S - 1) * tb_step, (i + S - 1) % S);
             umma::bulk_wait_read<SO - 1>();  // the stores of tile i - SO have read this output stage
         }
+        const int t0 = tb * kBulkTokens;
+        const int ta = t0 + part * kTokPerThread, tz = min(ta + kTokPerThread, a.T);
+        if (has_vec && ta < tz && (s < 0 || ta >= s_end)) enter(ta);  // overlaps the copy wait
         const bool ok = umma::mbar_wait(&full[st], (uint32_t)(i / S) & 1u, kVarPolls);
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
         }
-        const int t0 = tb * kBulkTokens;
-        const int ta = t0 + part * kTokPerThread, tz = min(ta + kTokPerThread, a.T);
         if (has_vec && ta < tz) {
             const ActT *rows = reinterpret_cast<const ActT *>(smem + st * Geo::STAGE) + (size_t)cv * V;
             // row of token t in the stage: t - t0 + W - 1
             auto row = [&](int t) { return rows + (size_t)(t - t0 + W - 1) * (kBulkVecs * V); };
-            int s = seq_of(a.cu, a.nseq, ta);
-            int s_end = a.cu[s + 1];
-            bool live = true;
             float win[W - 1][V];  // win[W-2]: the newest input before the current token
-            // window of token t of sequence s: inputs t-1..t-(W-1) from the tile when they belong
-            // to s, else from the sequence's stored window (zeros without one)
+            // window of token t of the current sequence: inputs t-1..t-(W-1) from the tile when they
+            // belong to it, else from the sequence's stored window (zeros without one)
             auto seed = [&](int t) {
-                const int32_t sl = a.slot ? a.slot[s] : -1;
-                live = sl >= -1 && sl < a.num_slots;
-                const bool has = a.conv_pool && sl >= 0 && live && a.init && a.init[s];
-                const ActT *sp = has ? static_cast<const ActT *>(a.conv_pool) + sl * a.conv_stride +
-                                           (int64_t)c0 * a.Wc
-                                     : nullptr;
-                const int begin = a.cu[s];
 #pragma unroll
                 for (int k = 1; k < W; ++k) {
-                    const int rel = t - k - begin;
+                    const int rel = t - k - s_begin;
                     if (rel >= 0) {
                         unpack16(*reinterpret_cast<const uint4 *>(row(t - k)), win[W - 1 - k]);
                     } else {
@@ -246,9 +255,8 @@ __global__ void __launch_bounds__(BulkGeom<W>::THREADS, BulkGeom<W>::MINB) k_con
                 }
             } else {
                 for (int t = ta; t < tz; ++t) {
-                    if (t >= s_end) {  // first token of a later sequence (empty ones are skipped)
-                        while (a.cu[s + 1] <= t) ++s;
-                        s_end = a.cu[s + 1];
+                    if (t >= s_end) {  // first token of a later sequence
+                        enter(t);
                         seed(t);
                     }
                     float x[V];
