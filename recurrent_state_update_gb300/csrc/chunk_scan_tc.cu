@@ -240,12 +240,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
             sv->cum2[tid] = run * LOG2E;
             sv->delta[tid] = dlt;
         }
-        // G = C B^T and Y_off = C h_prev^T
-        int bad = 0;
+        // G = C B^T and Y_off = C h_prev^T (every thread waits for the tiles itself: it reads X)
+        int bad = mbar_wait(&sv->bar_tma, ph, kPolls) ? 0 : 1;
         if (tid == 0) {
-            if (!mbar_wait(&sv->bar_tma, ph, kPolls)) {
-                bad = 1;
-            } else {
+            if (!bad) {
                 pending &= ~1u;
                 tc_fence_after();
                 const uint32_t c = smem_u32(sm + OFF_C), b = smem_u32(sm + OFF_B), hh = smem_u32(sm + OFF_H);
@@ -262,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
                 pend_par[1] = ph;
             }
         }
-        if (__syncthreads_or(bad)) {
+        if (__syncthreads_or(bad)) {  // cum visible; a tile copy that gave up ends the CTA
             failed = true;
             break;
         }
@@ -285,12 +283,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
 
         // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, written over the consumed C tile.
         // Row i = this thread's lane; this warp forms column blocks jb = hf and hf + 2.
-        bad = !mbar_wait(&sv->bar_g, ph, kPolls);
-        if (__syncthreads_or(bad)) {
-            failed = true;
-            break;
-        }
-        if (tid == 0) pending &= ~2u;
+        if (!mbar_wait(&sv->bar_g, ph, kPolls)) bad = 1;
+        else if (tid == 0) pending &= ~2u;
         tc_fence_after();
         {
             const float ci = sv->cum2[row];
@@ -329,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         __syncthreads();
         tc_fence_after();
         // Y_diag = M X (into the G columns, which are consumed)
-        if (tid == 0) {
+        if (tid == 0 && !bad) {
             const uint32_t m = smem_u32(sm + OFF_C), x = smem_u32(sm + OFF_X);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -347,12 +341,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
             for (int qq = 0; qq < 32; ++qq) v[qq] *= decay;
             tmem_st32(t_h + lane_base + c0, v);
         }
-        bad = !mbar_wait(&sv->bar_yd, ph, kPolls);
-        if (__syncthreads_or(bad)) {
-            failed = true;
-            break;
-        }
-        if (tid == 0) pending &= ~4u;
+        if (!mbar_wait(&sv->bar_yd, ph, kPolls)) bad = 1;
+        else if (tid == 0) pending &= ~4u;
         tc_fence_after();
         // w (.) X in place (the row of a 16-byte chunk is its byte offset / 128)
 #pragma unroll
@@ -375,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         __syncthreads();
         tc_fence_after();
         // h^T += B^T (w X)
-        if (tid == 0) {
+        if (tid == 0 && !bad) {
             const uint32_t b = smem_u32(sm + OFF_B), x = smem_u32(sm + OFF_X);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -422,14 +412,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
             }
         }
         // the state MMA must finish before the tiles are reloaded and the state is read
-        bad = !mbar_wait(&sv->bar_s, ph, kPolls);
-        if (__syncthreads_or(bad)) {
-            failed = true;
-            break;
-        }
+        if (!mbar_wait(&sv->bar_s, ph, kPolls)) bad = 1;
         tc_fence_after();
         h_valid = true;
-        if (tid == 0) {
+        if (tid == 0 && !bad) {
             pending &= ~8u;
             if (k + 1 < nsub) {
                 issue_loads(sm, sv, &mX, &mB, &mC, h, g, t0 + SQ);
@@ -462,7 +448,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(bad)) {  // an MMA wait that gave up anywhere in the CTA ends it here
+            failed = true;
+            break;
+        }
         tc_fence_after();
     }
     if (failed) {
