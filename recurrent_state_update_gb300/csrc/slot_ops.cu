@@ -227,13 +227,13 @@ __global__ void __launch_bounds__(1024) k_ckpt_store_int8(const QArgs a) {
     for (int p = sh; p < a.P; p += shares) {
         float v[8];
         load8(t + (int64_t)p * a.N, v);
-        uint32_t w[2] = {0u, 0u};
+        // nearest code (round half to even, as rint), clamped to +-127, four codes packed per word
+        int c[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float r = fminf(fmaxf(rintf(v[k] * rc[k]), -127.0f), 127.0f);
-            w[k >> 2] |= ((uint32_t)(int)r & 0xffu) << (8 * (k & 3));
-        }
-        *reinterpret_cast<uint2 *>(q + (int64_t)p * a.N) = make_uint2(w[0], w[1]);
+        for (int k = 0; k < 8; ++k) c[k] = max(-127, min(127, __float2int_rn(v[k] * rc[k])));
+        const uint32_t w0 = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+        const uint32_t w1 = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+        *reinterpret_cast<uint2 *>(q + (int64_t)p * a.N) = make_uint2(w0, w1);
     }
 }
 
