@@ -21,6 +21,8 @@
 //    values exchanged at each shuffle step) leaves one row total per lane pair.
 //  - The first head's state loads are issued before the conv phase so they are in flight
 //    while the CTA convolves.
+#include <mutex>
+
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -1276,6 +1278,63 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 // Persistent single-token launch: as many stages as fit beside the item buffers, one CTA per SM.
 // Returns 1 when the layer's conv / xBC / z segments are not 16-byte aligned for bulk copies (the
 // caller then uses the per-item kernel).
+// Whether a cluster of the configuration's size can be resident, remembered per (device, kernel,
+// cluster size, block, shared memory) so that small-batch calls do not repeat the occupancy query.
+static bool cluster_fits(const void *kern, const cudaLaunchConfig_t &cfg) {
+    struct Entry {
+        int dev;
+        const void *k;
+        unsigned cx, bx;
+        size_t smem;
+        bool ok;
+    };
+    static Entry cache[32];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const unsigned cx = cfg.attrs[0].val.clusterDim.x, bx = cfg.blockDim.x;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (int e = 0; e < used; ++e)
+            if (cache[e].dev == dev && cache[e].k == kern && cache[e].cx == cx && cache[e].bx == bx &&
+                cache[e].smem == cfg.dynamicSmemBytes)
+                return cache[e].ok;
+    }
+    int clusters = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters >= 1;
+    if (!ok) (void)cudaGetLastError();
+    std::lock_guard<std::mutex> g(mu);
+    if (used < 32) cache[used++] = {dev, kern, cx, bx, cfg.dynamicSmemBytes, ok};
+    return ok;
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at least `smem` bytes;
+// the attribute call is remembered per (device, kernel) so repeated launches skip it.
+static bool smem_limit(const void *kern, size_t smem) {
+    struct Entry {
+        int dev;
+        const void *k;
+        size_t smem;
+    };
+    static Entry cache[64];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> g(mu);
+    for (int e = 0; e < used; ++e)
+        if (cache[e].dev == dev && cache[e].k == kern && cache[e].smem >= smem) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+    for (int e = 0; e < used; ++e)
+        if (cache[e].dev == dev && cache[e].k == kern) {
+            cache[e].smem = smem;
+            return true;
+        }
+    if (used < 64) cache[used++] = {dev, kern, smem};
+    return true;
+}
+
 template <typename StateT, typename ActT, int P, int N>
 static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int LC = a.HG * P + 2 * N;
@@ -1316,8 +1375,7 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int W = a.batch * a.G;
     const int grid = W < sm_count ? W : sm_count;
     auto kern = k_decode_stream<StateT, ActT, P, N>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return MAMBA_ECUDA;
+    if (!smem_limit(reinterpret_cast<const void *>(kern), smem)) return MAMBA_ECUDA;
     kern<<<grid, kStreamThreads, smem, stream>>>(sa);
     return launch_status();
 }
@@ -1382,10 +1440,7 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
         }
     }
     auto kern = ntok == 1 ? k_decode<StateT, ActT, P, N, 1> : k_decode<StateT, ActT, P, N, 0>;
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return MAMBA_ECUDA;
-    }
+    if (smem > 48 * 1024 && !smem_limit(reinterpret_cast<const void *>(kern), smem)) return MAMBA_ECUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.G * ksplit, a.batch);
     cfg.blockDim = dim3(nhs * TL::TH);
@@ -1398,13 +1453,7 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (ksplit > 1) {
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-            (void)cudaGetLastError();
-            continue;  // no room for such a cluster: one CTA per (row, group)
-        }
-    }
+    if (ksplit > 1 && !cluster_fits(reinterpret_cast<const void *>(kern), cfg)) continue;  // one CTA per (row, group)
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
     }
