@@ -14,7 +14,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import device_normal_pool, f64, tile_rel_err, tile_rms_err, to_dev, to_i32
+from gpu_util import device_normal_pool, f64, tile_rel_err, tile_rms_err, to_dev, to_i32, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -357,3 +357,72 @@ def test_device_side_errors_leave_rows_untouched():
     assert int(err.item()) & bd.MAMBA_ERR_ACCEPT_RANGE
     assert torch.equal(ssm[3], ssm1[3]) and torch.equal(conv[3], conv1[3])
     assert torch.equal(ssm[4], ssm1[10])
+
+
+# Other compiled (head_dim, d_state) tiles, each through the launch paths a batch selects: a
+# small single-token batch splits a group's heads over a thread-block cluster, a batch of at
+# least two (row, group) items per SM takes the persistent stream kernel, several tokens or a
+# conv kernel other than 4 take the per-(row, group) kernel.
+#   (head_dim, d_state, heads, groups, conv kernel, state, activations, batch, tokens, spec columns)
+OTHER_TILES = [
+    (32, 64, 8, 2, 4, wl.BF16, wl.BF16, 3, 1, 0),
+    (32, 64, 8, 2, 4, wl.BF16, wl.BF16, 170, 1, 0),
+    (64, 64, 6, 3, 4, wl.F32, wl.BF16, 4, 1, 0),
+    (64, 64, 6, 3, 4, wl.F32, wl.BF16, 120, 1, 0),
+    (128, 128, 4, 1, 4, wl.BF16, wl.BF16, 2, 1, 0),
+    (128, 128, 4, 1, 4, wl.BF16, wl.BF16, 320, 1, 0),
+    (128, 128, 4, 2, 3, wl.F32, wl.F32, 5, 2, 2),
+    (32, 64, 8, 2, 4, wl.BF16, wl.BF16, 40, 3, 3),
+    (64, 128, 16, 2, 4, wl.BF16, wl.F32, 50, 1, 0),
+    (16, 16, 4, 1, 4, wl.BF16, wl.BF16, 400, 1, 0),
+]
+
+
+@pytest.mark.parametrize("P,N,H,G,W,state,act,batch,ntok,spec", OTHER_TILES)
+def test_other_compiled_tiles(P, N, H, G, W, state, act, batch, ntok, spec):
+    """Two decode calls in a row at a compiled tile other than the Nemotron one, 10 % of rows
+    padded; several-token calls write each token's state to a scratch slot.  Per call the
+    oracle starts from the GPU's own state, so the bf16 bound is the per-step one."""
+    import torch
+    seed = 300 + P + N + batch
+    shape = wl.LayerShape(nheads=H, head_dim=P, d_state=N, n_groups=G, conv_kernel=W, num_spec=spec)
+    S = batch * (1 + (ntok if spec else 0)) + 16
+    layer = Layer(shape, seed, act=act)
+    desc = bd.layer_desc(shape, state=state, act=act)
+    assert bd.mamba_decode_supported(desc) == bd.MAMBA_OK
+    st = wl.initial_states(wl.rng(seed, 2), shape, S, state, act)
+    ssm, conv = to_dev(st["ssm"], state), to_dev(st["conv"], act)
+    o_conv = wl.upcast(st["conv"], act)
+    ids = wl.rng(seed, 3).choice(S, size=batch * (1 + (ntok if spec else 0)), replace=False).astype(np.int32)
+    slot = ids[:batch].copy()
+    slot[wl.rng(seed, 4).choice(batch, size=int(round(0.1 * batch)), replace=False)] = -1
+    scratch = ids[batch:].reshape(batch, ntok) if spec else None
+    live = slot[slot >= 0]
+    state_tol = FP32_TOL if state == wl.F32 else BF16_STEP_TOL
+    y_tol = FP32_TOL if (state == wl.F32 and act == wl.F32) else 2e-2
+    for step in range(2):
+        ssm_before = ssm.clone()
+        o_ssm = f64(ssm)
+        dev, o = _step_inputs(layer, seed, step, batch, ntok=ntok)
+        y = torch.zeros(batch, ntok, H * P, device="cuda", dtype=torch_dtype(act))
+        _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y,
+                  scratch_t=None if scratch is None else to_i32(scratch))
+        torch.cuda.synchronize()
+        y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
+        got_y = f64(y)
+        rows = np.flatnonzero(slot >= 0)
+        assert tile_rel_err(got_y[rows].reshape(len(rows), ntok, H, P), y_o[rows].reshape(len(rows), ntok, H, P),
+                            1) < y_tol
+        assert not got_y[slot < 0].any()  # padded rows' outputs are not written
+        got_ssm = f64(ssm)
+        if scratch is None:
+            assert tile_rel_err(got_ssm[live], o_ssm[live], 2) < state_tol
+        else:
+            np.testing.assert_array_equal(got_ssm[live], f64(ssm_before)[live])  # main slots untouched
+            for j in range(ntok):
+                sj = scratch[slot >= 0, j]
+                assert tile_rel_err(got_ssm[sj], o_ssm[sj], 2) < state_tol
+        np.testing.assert_array_equal(f64(conv), o_conv)  # conv windows hold raw inputs, exactly
+        touched = set(live.tolist()) | (set() if scratch is None else set(scratch[slot >= 0].ravel().tolist()))
+        dead = np.array(sorted(set(range(S)) - touched), dtype=np.int64)
+        np.testing.assert_array_equal(got_ssm[dead], f64(ssm_before)[dead])

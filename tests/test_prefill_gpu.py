@@ -211,3 +211,24 @@ def test_prefill_bad_seqlens_flagged_nothing_written():
     assert int(err.item()) & bd.MAMBA_ERR_SEQLENS
     np.testing.assert_array_equal(f64(pr.pool), wl.upcast(pr.pool0, wl.F32))
     assert not f64(pr.y).any()
+
+
+@pytest.mark.parametrize("H,G", [(80, 1), (24, 3)])
+def test_prefill_tc_other_head_and_group_counts(H, G):
+    """Tensor-core path at head_dim 64, d_state 128 with other head and group counts (one group
+    shared by 80 heads, three groups of 8): ragged and empty sequences, initial states,
+    checkpoints, z gate."""
+    shape = wl.LayerShape(nheads=H, head_dim=64, d_state=128, n_groups=G)
+    pr = Problem(shape, [300, 0, 1025, 128], seed=10 + H, act=wl.BF16, state=wl.BF16, has_init=[1, 1, 0, 1],
+                 interval=512, with_z=True)
+    pr.run_gpu()
+    pr.check(2e-2)
+
+
+def test_prefill_portable_bf16():
+    """A shape the tensor-core path does not take (head_dim 16, d_state 32) with bf16 activations
+    and state: the portable chunked path, ragged sequences, checkpoints, z gate."""
+    pr = Problem(SMALL, [300, 1, 513, 64, 0], seed=12, act=wl.BF16, state=wl.BF16, has_init=[1, 0, 1, 1, 1],
+                 interval=256, with_z=True)
+    pr.run_gpu()
+    pr.check(2e-2)
