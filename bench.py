@@ -707,6 +707,14 @@ def run_prefill(torch, args, rank, world, dist, hbm_peak, bf16_peak):
     return prefill
 
 
+def decode_config(world, layers):
+    """The decode workload as both arms report it."""
+    return {"workload": DECODE["name"], "layers": layers, "global_batch": DECODE["batch"] * world,
+            "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
+            "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
+            "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"}
+
+
 def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_peak, peak_src, e2e, ck, prefill,
          cpu, spec=None, sweep=None, ckpt=None, m1=None):
     line = {
@@ -714,10 +722,7 @@ def emit(args, world, layers, ms, value, token_layers, achieved, launch_ms, hbm_
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": DECODE["name"], "layers": layers, "global_batch": DECODE["batch"] * world,
-                   "pool_slots": DECODE["pool"], "shape": "H128 P64 N128 G8 W4 (conv_dim 10240)",
-                   "state_dtype": "bf16", "parallelism": f"dp{world} (independent slot pools)",
-                   "l2": "no flush: each launch touches 512 MiB of state (> 129 MB L2)"},
+        "config": decode_config(world, layers),
         "token_layers_per_s": token_layers,
         "roofline": {"bound": "hbm", "kernel": "k_decode_stream", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_src,
@@ -745,8 +750,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = 8
-    # one step = the oracle on `rows` rows of one decode layer
+    rows = 32
+    # one step = the oracle on `rows` rows of one decode layer (a bounded sample of the workload)
     import oracle
     seed = DECODE["seed"] * 1000
     g = wl.rng(seed, 0)
@@ -779,7 +784,7 @@ def run_reference(args):
         "value": value, "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": DECODE["name"], "sample_rows_per_step": rows},
+        "config": dict(decode_config(1, DECODE["layers"]), sample_rows_per_step=rows),
         "token_layers_per_s": rows / (el / args.steps),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
