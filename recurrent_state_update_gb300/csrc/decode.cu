@@ -21,6 +21,7 @@
 //    values exchanged at each shuffle step) leaves one row total per lane pair.
 //  - The first head's state loads are issued before the conv phase so they are in flight
 //    while the CTA convolves.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1335,6 +1336,20 @@ static bool smem_limit(const void *kern, size_t smem) {
     return true;
 }
 
+// SM count of the current device, read once per device (0 if it cannot be read).
+static int device_sms() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> count[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = count[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <typename StateT, typename ActT, int P, int N>
 static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int LC = a.HG * P + 2 * N;
@@ -1362,13 +1377,8 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     if (ns < step || ns % step != 0) return 1;
     const size_t smem = StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total;
     if (smem > 227 * 1024) return 1;
-    static int sm_count = 0;
-    if (sm_count == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return MAMBA_ECUDA;
-    }
+    const int sm_count = device_sms();
+    if (sm_count <= 0) return MAMBA_ECUDA;
     StreamArgs sa;
     sa.d = a;
     sa.ns = ns;
@@ -1378,16 +1388,6 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     if (!smem_limit(reinterpret_cast<const void *>(kern), smem)) return MAMBA_ECUDA;
     kern<<<grid, kStreamThreads, smem, stream>>>(sa);
     return launch_status();
-}
-
-static int device_sms() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 0;
-    }
-    return n;
 }
 
 template <typename StateT, typename ActT, int P, int N>
