@@ -9,6 +9,7 @@ must pass, so a failure means the planted mistake was caught, not that the harne
 
 Nothing here touches the repository's own oracle build or the CUDA library.
 """
+import concurrent.futures
 import os
 import shutil
 import subprocess
@@ -90,28 +91,46 @@ def _copy_tree(dst):
 
 
 def _run_pins(dst):
-    env = dict(os.environ, PYTHONDONTWRITEBYTECODE="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q", "-p", "no:cacheprovider"],
-                       cwd=dst, env=env, capture_output=True, text=True, timeout=600)
+    # the copy's own directory on the path; no conftest (it only registers the GPU marker and
+    # would import torch in every one of these processes)
+    env = dict(os.environ, PYTHONDONTWRITEBYTECODE="1", PYTHONPATH=dst)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q", "-p", "no:cacheprovider",
+                        "--noconftest"], cwd=dst, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode, r.stdout + r.stderr
 
 
-def test_unchanged_copy_passes_the_pins(tmp_path):
-    _copy_tree(str(tmp_path))
-    rc, out = _run_pins(str(tmp_path))
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Pin-suite exit code and output for the unchanged copy and every planted mistake, run side
+    by side in separate processes (each copy builds its own oracle library)."""
+    cases = [("unchanged", None, None)] + MUTATIONS
+
+    def run(case):
+        what, old, new = case
+        dst = str(tmp_path_factory.mktemp("oracle_copy"))
+        _copy_tree(dst)
+        if old is not None:
+            src = os.path.join(dst, "oracle", "mamba_oracle.c")
+            text = open(src).read()
+            if old not in text:
+                return None, f"the oracle no longer contains the expression this case changes: {old}"
+            with open(src, "w") as f:
+                f.write(text.replace(old, new, 1))
+        return _run_pins(dst)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+        return dict(zip((c[0] for c in cases), ex.map(run, cases)))
+
+
+def test_unchanged_copy_passes_the_pins(outcomes):
+    rc, out = outcomes["unchanged"]
     assert rc == 0, out[-2000:]
 
 
-@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_fails_a_pin(tmp_path, what, old, new):
-    dst = str(tmp_path)
-    _copy_tree(dst)
-    src = os.path.join(dst, "oracle", "mamba_oracle.c")
-    text = open(src).read()
-    assert old in text, f"the oracle no longer contains the expression this case changes: {old}"
-    with open(src, "w") as f:
-        f.write(text.replace(old, new, 1))
-    rc, out = _run_pins(dst)
+@pytest.mark.parametrize("what", [m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(outcomes, what):
+    rc, out = outcomes[what]
+    assert rc is not None, out
     # exit code 1: the suite ran and a pin failed (a build or collection error would be 2 or more);
     # a negative code: the changed oracle crashed inside a pin (an index now runs past a buffer)
     assert (rc == 1 and " failed" in out) or rc < 0, f"{what}: no pin failed\n{out[-2000:]}"
