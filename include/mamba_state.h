@@ -103,6 +103,22 @@ int mamba_decode_supported(const mamba_layer_desc *desc);
 /* Human-readable name of a mamba_status. */
 const char *mamba_status_string(int status);
 
+/*
+ * mamba_check_slot_ids -- host-side check of one call's slot ids before they go to the device
+ * [P1 slot pool: a request owns one slot id; a padding row uses a reserved id].  HOST pointers:
+ *   slot_ids       (batch)       int32, -1 = padding row
+ *   scratch_slots  (batch, ntok) int32 or NULL, -1 = no write for that token; the entries of a
+ *                                padding row are ignored (the row writes nothing)
+ * Every id must be -1 or in [0, num_slots), and no id other than -1 may appear twice among the
+ * live rows' slot ids and scratch slots (the distinct-slot precondition of every call that
+ * writes the pool).  Returns MAMBA_OK, or MAMBA_EINVAL with *first_bad (may be NULL) set to
+ * the index of the first offending entry, scratch entry (i, j) counted as batch + i*ntok + j,
+ * or -1 when the arguments themselves are invalid.  Uses host memory of num_slots bytes for
+ * the duration of the call; touches no device memory.
+ */
+int mamba_check_slot_ids(const int32_t *slot_ids, int32_t batch, const int32_t *scratch_slots, int32_t ntok,
+                         int64_t num_slots, int64_t *first_bad);
+
 /* ---------------------------------------------------------------------------------------- */
 /* decode                                                                                   */
 /* ---------------------------------------------------------------------------------------- */

@@ -90,6 +90,7 @@ SIGNATURES = {
     "mamba_chunk_scan_noalloc": (ctypes.c_int, [_dp, _vp, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32,
                                                 _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mamba_chunk_scan_static_scratch_bytes": (_sz, []),
+    "mamba_check_slot_ids": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i64, ctypes.POINTER(_i64)]),
 }
 
 
@@ -157,6 +158,20 @@ def mamba_conv_state_bytes(desc: LayerDesc) -> int:
 
 def mamba_decode_supported(desc: LayerDesc) -> int:
     return lib().mamba_decode_supported(ctypes.byref(desc))
+
+
+def mamba_check_slot_ids(slot_ids, num_slots: int, scratch_slots=None) -> tuple[int, int]:
+    """Host-side check of one call's slot ids (numpy int32 arrays: (batch,) and (batch, ntok)).
+    Returns (status, index of the first offending entry or -1)."""
+    import numpy as np
+    ids = np.ascontiguousarray(slot_ids, dtype=np.int32)
+    sc = None if scratch_slots is None else np.ascontiguousarray(scratch_slots, dtype=np.int32)
+    ntok = 0 if sc is None else (sc.shape[1] if sc.ndim == 2 else 1)
+    bad = _i64(-1)
+    rc = lib().mamba_check_slot_ids(ids.ctypes.data if ids.size else None, int(ids.shape[0]),
+                                    None if sc is None else sc.ctypes.data, int(ntok), int(num_slots),
+                                    ctypes.byref(bad))
+    return rc, int(bad.value)
 
 
 def mamba_chunk_scan_workspace_bytes(desc: LayerDesc, total_tokens: int, nseq: int, chunk: int) -> int:

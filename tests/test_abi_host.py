@@ -250,3 +250,27 @@ def test_mamba1_host_errors(lib):
     assert call(dd=bd.mamba1_desc(5121, 16)) == bd.MAMBA_EINVAL
     r = lib.mamba1_conv_update(ctypes.byref(d), None, 5120 * 3, 8, FAKE, 4, 1, FAKE, FAKE, None, FAKE, None, None)
     assert r == bd.MAMBA_EINVAL
+
+
+def test_check_slot_ids(lib):
+    """Host-side slot-id check: range, padding, distinct ids across rows and scratch slots."""
+    import numpy as np
+    ok = np.array([3, -1, 0, 7], np.int32)
+    assert bd.mamba_check_slot_ids(ok, 8) == (bd.MAMBA_OK, -1)
+    assert bd.mamba_check_slot_ids(np.array([3, 8], np.int32), 8) == (bd.MAMBA_EINVAL, 1)      # outside the pool
+    assert bd.mamba_check_slot_ids(np.array([3, -2], np.int32), 8) == (bd.MAMBA_EINVAL, 1)     # below -1
+    assert bd.mamba_check_slot_ids(np.array([5, -1, 5], np.int32), 8) == (bd.MAMBA_EINVAL, 2)  # used twice
+    assert bd.mamba_check_slot_ids(np.array([-1, -1], np.int32), 8) == (bd.MAMBA_OK, -1)       # padding repeats
+    assert bd.mamba_check_slot_ids(np.zeros(0, np.int32), 8) == (bd.MAMBA_OK, -1)
+    # scratch slots: (batch, ntok); entry (i, j) is reported as batch + i*ntok + j
+    rows = np.array([0, 1, -1], np.int32)
+    scratch = np.array([[2, 3], [4, -1], [0, 1]], np.int32)  # the padding row's entries are ignored
+    assert bd.mamba_check_slot_ids(rows, 8, scratch) == (bd.MAMBA_OK, -1)
+    scratch[1, 1] = 2  # row 1 token 1 reuses row 0's scratch slot
+    assert bd.mamba_check_slot_ids(rows, 8, scratch) == (bd.MAMBA_EINVAL, 3 + 1 * 2 + 1)
+    scratch[1, 1] = 1  # a scratch slot equal to a live row's own slot
+    assert bd.mamba_check_slot_ids(rows, 8, scratch) == (bd.MAMBA_EINVAL, 3 + 1 * 2 + 1)
+    # invalid arguments
+    bad = ctypes.c_int64(0)
+    assert lib.mamba_check_slot_ids(None, 2, None, 0, 8, ctypes.byref(bad)) == bd.MAMBA_EINVAL and bad.value == -1
+    assert lib.mamba_check_slot_ids(ok.ctypes.data, 4, None, 0, 0, None) == bd.MAMBA_EINVAL
