@@ -119,6 +119,18 @@ const char *mamba_status_string(int status);
 int mamba_check_slot_ids(const int32_t *slot_ids, int32_t batch, const int32_t *scratch_slots, int32_t ntok,
                          int64_t num_slots, int64_t *first_bad);
 
+/*
+ * mamba_selftest_wait_timeout -- diagnostic of this library's failure path (the pages have no
+ * counterpart).  Every kernel here bounds each wait on its asynchronous copies and matrix
+ * operations (2^18 mbarrier polls, about one second on GB300) and reports a wait that runs out as
+ * MAMBA_ERR_TIMEOUT instead of hanging.  This call launches one small kernel that waits, with the same bounded wait, on a
+ * barrier phase nothing completes: after about one second it gives up, ORs MAMBA_ERR_TIMEOUT
+ * into *err_word (device int32, required) and stores the wait's duration in nanoseconds into
+ * *elapsed_ns (device uint64, may be NULL).  It touches nothing else, and the CUDA context stays
+ * usable.  Asynchronous on stream.
+ */
+int mamba_selftest_wait_timeout(int32_t *err_word, uint64_t *elapsed_ns, void *stream);
+
 /* ---------------------------------------------------------------------------------------- */
 /* decode                                                                                   */
 /* ---------------------------------------------------------------------------------------- */

@@ -91,6 +91,7 @@ SIGNATURES = {
                                                 _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mamba_chunk_scan_static_scratch_bytes": (_sz, []),
     "mamba_check_slot_ids": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i64, ctypes.POINTER(_i64)]),
+    "mamba_selftest_wait_timeout": (ctypes.c_int, [_vp, _vp, _vp]),
 }
 
 
@@ -158,6 +159,12 @@ def mamba_conv_state_bytes(desc: LayerDesc) -> int:
 
 def mamba_decode_supported(desc: LayerDesc) -> int:
     return lib().mamba_decode_supported(ctypes.byref(desc))
+
+
+def mamba_selftest_wait_timeout(err_word, elapsed_ns=None, stream=None):
+    """Diagnostic: one bounded wait that runs out (err_word: device int32; elapsed_ns: device int64)."""
+    _check(lib().mamba_selftest_wait_timeout(_ptr(err_word), _ptr(elapsed_ns), _stream(stream)),
+           "mamba_selftest_wait_timeout")
 
 
 def mamba_check_slot_ids(slot_ids, num_slots: int, scratch_slots=None) -> tuple[int, int]:

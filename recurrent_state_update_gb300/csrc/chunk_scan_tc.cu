@@ -34,7 +34,7 @@ constexpr int SQ = 128;  // tokens per sub-chunk (MMA M)
 constexpr int TP = 64;   // head_dim
 constexpr int TN = 128;  // d_state
 constexpr uint32_t BLK = 16384;  // one 128-row x 128-byte swizzled block
-constexpr uint32_t kPolls = 1u << 24;
+constexpr uint32_t kPolls = umma::kWaitPolls;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // shared-memory map (from a 1024-aligned base)

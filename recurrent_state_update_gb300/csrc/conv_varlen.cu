@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kVarThreads = 128;   // threads of the state write-back kernel
 constexpr int kBulkVecs = 128;     // 16-byte channel vectors per tile row (2 KB)
-constexpr uint32_t kVarPolls = 1u << 24;
+constexpr uint32_t kVarPolls = umma::kWaitPolls;
 
 struct VarlenArgs {
     const int32_t *cu;

@@ -334,7 +334,7 @@ struct DecodeArgs {
 };
 
 // Bound on the polls of one mbarrier wait (a copy that never lands is reported, not waited on forever).
-constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr uint32_t kMaxPolls = umma::kWaitPolls;
 constexpr int kFlagWords = 16;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }

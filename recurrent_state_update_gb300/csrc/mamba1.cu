@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kM1Threads, N <= 16 ? 3 : 1) k_mamba1_update(c
 // bytes) and an empty barrier (every consumer has used the stage).  All waits are bounded.
 
 constexpr int kM1StreamThreads = kM1Threads + 32;
-constexpr uint32_t kM1Polls = 1u << 24;
+constexpr uint32_t kM1Polls = umma::kWaitPolls;
 
 __host__ __device__ inline uint32_t m1_al16(uint32_t v) { return (v + 15u) & ~15u; }
 

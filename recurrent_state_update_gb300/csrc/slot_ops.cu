@@ -30,7 +30,7 @@ constexpr int kCopyBytes = kCopyThreads * 16 * 4;  // bytes one copy block moves
 constexpr int kQThreads = 128;
 constexpr int kStoreHeads = 1;           // heads quantised by one store block (more blocks in flight)
 constexpr int kLoadRows = 8;             // rows per thread and pass of the load
-constexpr uint32_t kQPolls = 1u << 24;  // bound on the wait for a staged tile
+constexpr uint32_t kQPolls = umma::kWaitPolls;  // bound on the wait for a staged tile
 
 inline size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 

@@ -49,6 +49,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Poll bound of every mbarrier wait in this library.  A poll that fails suspends the thread for a
+// few microseconds (3.75 us measured on GB300), so 2^18 polls give up after about one second; a
+// poll count, unlike a wall-clock limit, does not run down while the GPU is time-sliced away.
+constexpr uint32_t kWaitPolls = 1u << 18;
+
 // Waits for phase `parity` of `bar` with an upper bound on the number of polls; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t max_polls) {
     for (uint32_t i = 0; i < max_polls; ++i)

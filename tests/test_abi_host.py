@@ -274,3 +274,7 @@ def test_check_slot_ids(lib):
     bad = ctypes.c_int64(0)
     assert lib.mamba_check_slot_ids(None, 2, None, 0, 8, ctypes.byref(bad)) == bd.MAMBA_EINVAL and bad.value == -1
     assert lib.mamba_check_slot_ids(ok.ctypes.data, 4, None, 0, 0, None) == bd.MAMBA_EINVAL
+
+
+def test_selftest_wait_timeout_needs_an_error_word(lib):
+    assert lib.mamba_selftest_wait_timeout(None, None, None) == bd.MAMBA_EINVAL
