@@ -724,3 +724,36 @@ def test_input_recipe_ranges():
     assert (ids == -1).sum() == round(0.1 * 1024)
     live = ids[ids >= 0]
     assert len(np.unique(live)) == len(live)
+
+
+def test_align_mode_page_example():
+    """The page's align-mode example (tests/golden/align_mode_example.txt): checkpoints of a
+    4000-token prompt at 1280-token blocks sit at 1280, 2560 and 3840; a request that extends the
+    prompt by 200 tokens resumes from the 3840-token state, and replaying its last 360 tokens
+    (chunks of 256 and 104) from that state equals prefilling all of its 4200 tokens in one pass."""
+    gold = _golden("align_mode_example.txt")
+    n_prompt, block = int(gold["prompt_tokens"]), int(gold["block_tokens"])
+    n_b = n_prompt + int(gold["private_tokens"])
+    chunk = int(gold["chunk_tokens"])
+    pr = _random_problem(70, H=2, P=3, N=4, G=1, T=n_b)
+    h0 = pr["h0"][None]
+    max_ckpt = n_prompt // block + 1
+    # the first request: its prompt only, checkpoints every block
+    _, _, hc = oracle.prefill_steps(np.array([0, n_prompt], np.int32), pr["x"][:n_prompt], pr["dt"][:n_prompt],
+                                    pr["A"], pr["B"][:n_prompt], pr["C"][:n_prompt], h0=h0, D=pr["D"],
+                                    dt_bias=pr["dt_bias"], ckpt_interval=block, max_ckpt=max_ckpt)
+    kept = [block * (k + 1) for k in range(max_ckpt) if not np.isnan(hc[0, k]).any()]
+    assert kept == [int(v) for v in gold["checkpoints"].split()]
+    hit = max(p for p in kept if p <= n_prompt)
+    assert hit == int(gold["hit_tokens"]) and n_b - hit == int(gold["recomputed_tokens"])
+    # the second request in one pass, and resumed from the checkpoint at `hit`
+    y_one, h_one, _ = oracle.prefill_steps(np.array([0, n_b], np.int32), pr["x"], pr["dt"], pr["A"], pr["B"],
+                                           pr["C"], h0=h0, D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    r = slice(hit, n_b)
+    h_hit = hc[0, kept.index(hit)]
+    y_rep, h_rep = oracle.prefill_chunked(pr["x"][r], pr["dt"][r], pr["A"], pr["B"][r], pr["C"][r], chunk=chunk,
+                                          h0=h_hit, D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"][r])
+    np.testing.assert_allclose(y_rep, y_one[r], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(h_rep, h_one[0], rtol=1e-11, atol=1e-12)
+    n_rep = n_b - hit
+    assert [min(chunk, n_rep - c0) for c0 in range(0, n_rep, chunk)] == [int(v) for v in gold["replay_chunks"].split()]
