@@ -6,7 +6,9 @@ None for nullable arguments), passes their device pointers and sizes, and raises
 no CPU path.  Loading fails loudly when the library has not been built.
 
 Layouts are the ones the C header documents (include/mamba_state.h); tensors must be
-contiguous except the pools, whose slot stride is taken from ``stride(0)``.
+contiguous except the pools, whose slot stride is taken from ``stride(0)``.  Each tensor's
+dtype is checked against the layer descriptor before its pointer is passed (ValueError), since
+the C ABI sees only addresses.
 """
 from __future__ import annotations
 
@@ -135,6 +137,26 @@ def _cptr(t):
     return _ptr(t)
 
 
+def _code_dtype(code):
+    import torch
+    return torch.bfloat16 if code == MAMBA_BF16 else torch.float32
+
+
+def _expect(what, **tensors):
+    """Raises ValueError when a tensor's dtype is not the one the call reads it as.  Each keyword
+    is (tensor or None, the torch dtype the library expects)."""
+    for name, (t, want) in tensors.items():
+        if t is not None and t.dtype != want:
+            raise ValueError(f"{what}: {name} must be {want}, got {t.dtype}")
+
+
+def _layer_dtypes(desc):
+    """(state, conv, activations, dt, fp32, int32, uint8) torch dtypes of a Mamba2 or Mamba1 desc."""
+    import torch
+    return (_code_dtype(desc.state_dtype), _code_dtype(desc.conv_dtype), _code_dtype(desc.act_dtype),
+            _code_dtype(desc.dt_dtype), torch.float32, torch.int32, torch.uint8)
+
+
 def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -192,6 +214,9 @@ def mamba_chunk_scan_workspace_bytes(desc: LayerDesc, total_tokens: int, nseq: i
 def mamba_conv_update(desc: LayerDesc, conv_pool, slot_ids, xbc_in, conv_w, xbc_out, *, conv_b=None,
                       err_word=None, stream=None):
     """Causal conv1d + SiLU over (batch, ntok, conv_dim) inputs, conv state updated in place."""
+    _, cv, act, _, f32, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_conv_update", conv_pool=(conv_pool, cv), slot_ids=(slot_ids, i32), xbc_in=(xbc_in, act),
+            conv_w=(conv_w, f32), xbc_out=(xbc_out, act), conv_b=(conv_b, f32), err_word=(err_word, i32))
     batch, ntok = int(slot_ids.shape[0]), int(xbc_in.shape[1])
     rc = lib().mamba_conv_update(ctypes.byref(desc), _ptr(conv_pool), conv_pool.stride(0), conv_pool.shape[0],
                                  _cptr(slot_ids), batch, ntok, _cptr(xbc_in), _cptr(conv_w), _cptr(conv_b),
@@ -203,6 +228,11 @@ def mamba_state_update(desc: LayerDesc, ssm_pool, slot_ids, xbc, dt, A, y, *, co
                        conv_b=None, scratch_slots=None, D=None, dt_bias=None, dt_softplus=True, z=None,
                        err_word=None, stream=None):
     """The batched decode step (conv fused when ``conv_pool`` is given), in place on the pools."""
+    st, cv, act, dtt, f32, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_state_update", ssm_pool=(ssm_pool, st), slot_ids=(slot_ids, i32), xbc=(xbc, act), dt=(dt, dtt),
+            A=(A, f32), y=(y, act), conv_pool=(conv_pool, cv), conv_w=(conv_w, f32), conv_b=(conv_b, f32),
+            scratch_slots=(scratch_slots, i32), D=(D, f32), dt_bias=(dt_bias, f32), z=(z, act),
+            err_word=(err_word, i32))
     batch, ntok = int(slot_ids.shape[0]), int(xbc.shape[1])
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
     rc = lib().mamba_state_update(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
@@ -216,6 +246,9 @@ def mamba_state_update(desc: LayerDesc, ssm_pool, slot_ids, xbc, dt, A, y, *, co
 def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept_len, *, conv_pool=None,
                       err_word=None, stream=None):
     """Keep accept_len[i] of the speculative tokens: copy the scratch state, re-seat the conv window."""
+    st, cv, _, _, _, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_spec_commit", ssm_pool=(ssm_pool, st), slot_ids=(slot_ids, i32), scratch_slots=(scratch_slots, i32),
+            accept_len=(accept_len, i32), conv_pool=(conv_pool, cv), err_word=(err_word, i32))
     batch, ntok = int(scratch_slots.shape[0]), int(scratch_slots.shape[1])
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
     rc = lib().mamba_spec_commit(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
@@ -231,6 +264,9 @@ def mamba_spec_commit(desc: LayerDesc, ssm_pool, slot_ids, scratch_slots, accept
 def mamba1_conv_update(desc: Mamba1Desc, conv_pool, slot_ids, x_in, conv_w, x_out, *, conv_b=None, err_word=None,
                        stream=None):
     """Causal conv1d + SiLU of a Mamba1 layer over (batch, ntok, d_inner) inputs, conv state in place."""
+    _, cv, act, _, f32, i32, _ = _layer_dtypes(desc)
+    _expect("mamba1_conv_update", conv_pool=(conv_pool, cv), slot_ids=(slot_ids, i32), x_in=(x_in, act),
+            conv_w=(conv_w, f32), x_out=(x_out, act), conv_b=(conv_b, f32), err_word=(err_word, i32))
     batch, ntok = int(slot_ids.shape[0]), int(x_in.shape[1])
     rc = lib().mamba1_conv_update(ctypes.byref(desc), _ptr(conv_pool), conv_pool.stride(0), conv_pool.shape[0],
                                   _cptr(slot_ids), batch, ntok, _cptr(x_in), _cptr(conv_w), _cptr(conv_b),
@@ -241,6 +277,10 @@ def mamba1_conv_update(desc: Mamba1Desc, conv_pool, slot_ids, x_in, conv_w, x_ou
 def mamba1_state_update(desc: Mamba1Desc, ssm_pool, slot_ids, x, dt, A, B, C, y, *, D=None, dt_bias=None,
                         dt_softplus=True, z=None, err_word=None, stream=None):
     """The batched single-token Mamba1 decode step, in place on the (slots, d_inner, d_state) pool."""
+    st, _, act, dtt, f32, i32, _ = _layer_dtypes(desc)
+    _expect("mamba1_state_update", ssm_pool=(ssm_pool, st), slot_ids=(slot_ids, i32), x=(x, act), dt=(dt, dtt),
+            A=(A, f32), B=(B, act), C=(C, act), y=(y, act), D=(D, f32), dt_bias=(dt_bias, f32), z=(z, act),
+            err_word=(err_word, i32))
     batch = int(slot_ids.shape[0])
     rc = lib().mamba1_state_update(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
                                    _cptr(slot_ids), batch, _cptr(x), _cptr(dt), _cptr(A), _cptr(B), _cptr(C), _cptr(D),
@@ -255,6 +295,9 @@ def mamba1_state_update(desc: Mamba1Desc, ssm_pool, slot_ids, x, dt, A, B, C, y,
 
 def mamba_slot_copy(desc: LayerDesc, ssm_pool, src_slots, dst_slots, *, conv_pool=None, err_word=None, stream=None):
     """Copy whole slot states src_slots[i] -> dst_slots[i] (checkpoint restore, copy-on-write)."""
+    st, cv, _, _, _, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_slot_copy", ssm_pool=(ssm_pool, st), src_slots=(src_slots, i32), dst_slots=(dst_slots, i32),
+            conv_pool=(conv_pool, cv), err_word=(err_word, i32))
     n = int(src_slots.shape[0])
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
     rc = lib().mamba_slot_copy(ctypes.byref(desc), _ptr(ssm_pool), ssm_pool.stride(0), ssm_pool.shape[0],
@@ -270,6 +313,9 @@ def mamba_int8_entry_bytes(desc: LayerDesc) -> int:
 def mamba_ckpt_store_int8(desc: LayerDesc, ssm_pool, src_slots, dst_entries, store, *, conv_pool=None,
                           err_word=None, stream=None):
     """Quantise slots into int8 store entries (per-(head, d_state channel) symmetric scales)."""
+    st, cv, _, _, _, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_ckpt_store_int8", ssm_pool=(ssm_pool, st), src_slots=(src_slots, i32),
+            dst_entries=(dst_entries, i32), conv_pool=(conv_pool, cv), err_word=(err_word, i32))
     n = int(src_slots.shape[0])
     eb = mamba_int8_entry_bytes(desc)
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
@@ -283,6 +329,9 @@ def mamba_ckpt_store_int8(desc: LayerDesc, ssm_pool, src_slots, dst_entries, sto
 def mamba_ckpt_load_int8(desc: LayerDesc, ssm_pool, src_entries, dst_slots, store, *, conv_pool=None,
                          err_word=None, stream=None):
     """Dequantise int8 store entries into slots."""
+    st, cv, _, _, _, i32, _ = _layer_dtypes(desc)
+    _expect("mamba_ckpt_load_int8", ssm_pool=(ssm_pool, st), src_entries=(src_entries, i32),
+            dst_slots=(dst_slots, i32), conv_pool=(conv_pool, cv), err_word=(err_word, i32))
     n = int(src_entries.shape[0])
     eb = mamba_int8_entry_bytes(desc)
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
@@ -301,6 +350,10 @@ def mamba_conv_varlen(desc: LayerDesc, cu_seqlens, xbc, conv_w, x_out, B_out, C_
                       slot_ids=None, has_initial_state=None, conv_b=None, err_word=None, stream=None):
     """Varlen causal conv1d + SiLU of a prefill batch into x | B | C, continuing each sequence
     from its conv state and writing the state back (when ``conv_pool`` is given)."""
+    _, cv, act, _, f32, i32, u8 = _layer_dtypes(desc)
+    _expect("mamba_conv_varlen", cu_seqlens=(cu_seqlens, i32), xbc=(xbc, act), conv_w=(conv_w, f32), x_out=(x_out, act),
+            B_out=(B_out, act), C_out=(C_out, act), conv_pool=(conv_pool, cv), slot_ids=(slot_ids, i32),
+            has_initial_state=(has_initial_state, u8), conv_b=(conv_b, f32), err_word=(err_word, i32))
     nseq = int(cu_seqlens.shape[0]) - 1
     total = int(xbc.shape[0])
     conv_stride = conv_pool.stride(0) if conv_pool is not None else 0
@@ -316,6 +369,10 @@ def mamba_chunk_scan(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x, dt, A, 
                      has_initial_state=None, ckpt_slots=None, ckpt_interval=0, chunk=256, D=None, dt_bias=None,
                      dt_softplus=True, z=None, err_word=None, stream=None):
     """Varlen chunked prefill (SSD form); final states and checkpoints written into the pool."""
+    st, _, act, dtt, f32, i32, u8 = _layer_dtypes(desc)
+    _expect("mamba_chunk_scan", ssm_pool=(ssm_pool, st), cu_seqlens=(cu_seqlens, i32), slot_ids=(slot_ids, i32), x=(x, act),
+            dt=(dt, dtt), A=(A, f32), B=(B, act), C=(C, act), y=(y, act), has_initial_state=(has_initial_state, u8),
+            ckpt_slots=(ckpt_slots, i32), D=(D, f32), dt_bias=(dt_bias, f32), z=(z, act), err_word=(err_word, i32))
     nseq = int(cu_seqlens.shape[0]) - 1
     total = int(x.shape[0])
     max_ckpt = int(ckpt_slots.shape[1]) if ckpt_slots is not None else 0
@@ -338,6 +395,10 @@ def mamba_chunk_scan_noalloc(desc: LayerDesc, ssm_pool, cu_seqlens, slot_ids, x,
                              dt_bias=None, dt_softplus=True, z=None, err_word=None, stream=None):
     """mamba_chunk_scan for callers that cannot allocate: the library's fixed scratch is used
     instead of a caller workspace (see the C header for its size limit and sharing rules)."""
+    st, _, act, dtt, f32, i32, u8 = _layer_dtypes(desc)
+    _expect("mamba_chunk_scan_noalloc", ssm_pool=(ssm_pool, st), cu_seqlens=(cu_seqlens, i32), slot_ids=(slot_ids, i32), x=(x, act),
+            dt=(dt, dtt), A=(A, f32), B=(B, act), C=(C, act), y=(y, act), has_initial_state=(has_initial_state, u8),
+            ckpt_slots=(ckpt_slots, i32), D=(D, f32), dt_bias=(dt_bias, f32), z=(z, act), err_word=(err_word, i32))
     nseq = int(cu_seqlens.shape[0]) - 1
     total = int(x.shape[0])
     max_ckpt = int(ckpt_slots.shape[1]) if ckpt_slots is not None else 0

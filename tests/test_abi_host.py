@@ -278,3 +278,27 @@ def test_check_slot_ids(lib):
 
 def test_selftest_wait_timeout_needs_an_error_word(lib):
     assert lib.mamba_selftest_wait_timeout(None, None, None) == bd.MAMBA_EINVAL
+
+
+def test_binding_rejects_tensors_of_the_wrong_dtype():
+    """The binding checks each tensor's dtype against the layer descriptor before it passes a
+    pointer (checked here with host tensors: the check comes before any device access)."""
+    import torch
+    shape = wl.TINY
+    desc = bd.layer_desc(shape)  # bf16 state and activations, fp32 dt
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    ok = dict(ssm_pool=torch.zeros(2, 4, 16, 16, dtype=bf), slot_ids=torch.zeros(1, dtype=i32),
+              xbc=torch.zeros(1, 1, shape.conv_dim, dtype=bf), dt=torch.zeros(1, 1, 4, dtype=f32),
+              A=torch.zeros(4, dtype=f32), y=torch.zeros(1, 1, 64, dtype=bf))
+    for name, bad in (("ssm_pool", torch.zeros(2, 4, 16, 16, dtype=f32)), ("slot_ids", torch.zeros(1, dtype=torch.int64)),
+                      ("xbc", torch.zeros(1, 1, shape.conv_dim, dtype=f32)), ("dt", torch.zeros(1, 1, 4, dtype=bf)),
+                      ("y", torch.zeros(1, 1, 64, dtype=f32))):
+        args = dict(ok, **{name: bad})
+        with pytest.raises(ValueError, match=f"mamba_state_update: {name} must be"):
+            bd.mamba_state_update(desc, args["ssm_pool"], args["slot_ids"], args["xbc"], args["dt"], args["A"],
+                                  args["y"])
+    with pytest.raises(ValueError, match="mamba_chunk_scan: has_initial_state must be"):
+        bd.mamba_chunk_scan(desc, ok["ssm_pool"], torch.zeros(2, dtype=i32), ok["slot_ids"],
+                            torch.zeros(1, 4, 16, dtype=bf), torch.zeros(1, 4, dtype=f32), ok["A"],
+                            torch.zeros(1, 1, 16, dtype=bf), torch.zeros(1, 1, 16, dtype=bf),
+                            torch.zeros(1, 4, 16, dtype=bf), None, has_initial_state=torch.zeros(1, dtype=torch.bool))

@@ -92,8 +92,9 @@ def test_noalloc_refuses_a_problem_larger_than_its_scratch():
     T = 8192  # 32 chunks of per-chunk fp32 states: more than the fixed scratch holds
     assert bd.mamba_chunk_scan_workspace_bytes(desc, T, 1, 256) > limit
     one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f = torch.zeros(1, dtype=torch.float32, device="cuda")  # placeholders: the call is refused before any launch
     pool = torch.zeros(1, 128, 64, 128, dtype=torch.float32, device="cuda")
     x = torch.zeros(T, 128, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(bd.MambaError) as e:
-        bd.mamba_chunk_scan_noalloc(desc, pool, to_i32(np.array([0, T])), one, x, one, one, one, one, x)
+        bd.mamba_chunk_scan_noalloc(desc, pool, to_i32(np.array([0, T])), one, x, f, f, f, f, x)
     assert e.value.status == bd.MAMBA_ENOSPACE
