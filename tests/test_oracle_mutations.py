@@ -31,7 +31,21 @@ MUTATIONS = [
     ("dt_bias dropped", "double s = dt + (dt_bias ? dt_bias[head] : 0.0);", "double s = dt;"),
     ("heads mapped to groups round-robin", "const int g = hh / (c->H / c->G);", "const int g = hh % c->G;"),
     ("gate z without SiLU", "if (z) yv *= silu(z[xi]);", "if (z) yv *= z[xi];"),
+    ("softplus replaced by exp below zero", "s > 0.0 ? s + log1p(exp(-s)) : log1p(exp(s))",
+     "s > 0.0 ? s + log1p(exp(-s)) : exp(s)"),
+    ("sigmoid of the negative branch inverted", "return e / (1.0 + e);", "return 1.0 / (1.0 + e);"),
+    # the slot pool: scratch slots of a speculative step and the commit
+    ("every scratch slot gets the last token's state",
+     "memcpy(c->ssm_pool + (int64_t)d * c->ssm_stride, h_tok + (int64_t)j * HPN,",
+     "memcpy(c->ssm_pool + (int64_t)d * c->ssm_stride, h_tok + (int64_t)(c->ntok - 1) * HPN,"),
+    ("commit copies the state one token early",
+     "ssm_pool + (int64_t)scratch[(int64_t)i * ntok + (a - 1)] * ssm_stride,",
+     "ssm_pool + (int64_t)scratch[(int64_t)i * ntok + (a > 1 ? a - 2 : 0)] * ssm_stride,"),
+    ("commit moves the conv window by the accepted count", "const int shift = ntok - a;", "const int shift = a;"),
     # causal conv1d over the conv state (the conv-state FIFO of the most recent inputs)
+    ("conv bias dropped", "double v = b ? b[c] : 0.0;", "double v = 0.0;"),
+    ("conv state keeps the output instead of the input", "st[Wc - 1] = u[(int64_t)j * Cd + c];",
+     "st[Wc - 1] = out[(int64_t)j * Cd + c];"),
     ("conv taps reversed", "v += w[(int64_t)c * W + k] * st[Wc - (W - 1) + k];",
      "v += w[(int64_t)c * W + (W - 2 - k)] * st[Wc - (W - 1) + k];"),
     ("conv window shifted by one too few",
@@ -105,9 +119,12 @@ def outcomes(tmp_path_factory):
     by side in separate processes (each copy builds its own oracle library)."""
     cases = [("unchanged", None, None)] + MUTATIONS
 
-    def run(case):
-        what, old, new = case
-        dst = str(tmp_path_factory.mktemp("oracle_copy"))
+    # the copies' directories are made here, one at a time (making numbered directories from
+    # several threads at once races)
+    dirs = [str(tmp_path_factory.mktemp("oracle_copy")) for _ in cases]
+
+    def run(job):
+        (what, old, new), dst = job
         _copy_tree(dst)
         if old is not None:
             src = os.path.join(dst, "oracle", "mamba_oracle.c")
@@ -119,7 +136,7 @@ def outcomes(tmp_path_factory):
         return _run_pins(dst)
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        return dict(zip((c[0] for c in cases), ex.map(run, cases)))
+        return dict(zip((c[0] for c in cases), ex.map(run, zip(cases, dirs))))
 
 
 def test_unchanged_copy_passes_the_pins(outcomes):
