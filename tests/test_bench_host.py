@@ -67,3 +67,45 @@ def test_max_over_ranks_on_two_gloo_ranks(tmp_path):
     mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
     for r in range(2):
         assert float((tmp_path / f"r{r}").read_text()) == 7.5
+
+
+REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "e2e", "gpu_launches", "cpu_baseline")
+
+
+def test_emitted_line_keeps_the_contract(capsys):
+    """The JSON line bench.py prints carries every key of the benchmark contract, with the
+    roofline, end-to-end, clocks and CPU-baseline objects in their documented shapes."""
+    import argparse
+    import json
+    args = argparse.Namespace(steps=100, warmup=5)
+    e2e = {"value": 5.8e3, "unit": "GB/s", "ms_per_step": 9.3, "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 2}
+    ck = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 20, "reasons": []}
+    cpu = {"value": 20.0, "unit": "GB/s", "cores": 16, "kind": "oracle", "sample": "32 rows"}
+    bench.emit(args, 1, 48, 9.0, 6.0e3, 1.3e6, 6.0e3, 0.1875, 6795.1, "measured", e2e, ck, None, cpu)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in REQUIRED:
+        assert k in line, k
+    assert line["config"]["workload"] and line["higher_is_better"] is True and line["scaling"] == "weak"
+    r = line["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert "traffic" in r
+    assert set(("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")) <= set(line["e2e"])
+    assert set(("sm_mhz", "sm_max_mhz", "reasons")) <= set(line["clocks"])
+    assert set(("value", "unit", "cores", "kind", "sample")) <= set(line["cpu_baseline"])
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """bench.py --impl reference: the oracle on the host cores, with the decode arm's metric,
+    unit and config (plus its sample), and an e2e object with no host-device bytes."""
+    import json
+    monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"])
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    for k in REQUIRED:
+        assert k in line, k
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"] == bench.decode_config(1, bench.DECODE["layers"])["workload"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
