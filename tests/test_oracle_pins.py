@@ -757,3 +757,46 @@ def test_align_mode_page_example():
     np.testing.assert_allclose(h_rep, h_one[0], rtol=1e-11, atol=1e-12)
     n_rep = n_b - hit
     assert [min(chunk, n_rep - c0) for c0 in range(0, n_rep, chunk)] == [int(v) for v in gold["replay_chunks"].split()]
+
+
+# ----------------------------------------------------------------------------------------
+# structural properties of the recurrence (each form: decode steps, step recurrence, chunks)
+# ----------------------------------------------------------------------------------------
+
+def _run_chunked_path(pr, h0, **kw):
+    kw.pop("dt_softplus", None)
+    y, hf = oracle.prefill_chunked(pr["x"], pr["dt"], pr["A"], pr["B"], pr["C"], chunk=3, h0=h0, **kw)
+    return hf, y
+
+
+@pytest.mark.parametrize("path", [_run_decode_path, _run_prefill_path, _run_chunked_path])
+def test_linear_in_initial_state_and_input(path):
+    """For fixed steps, B and C the update is linear in (h0, x): the decay and the input term
+    h <- exp(Delta A) h + Delta x B^T, the readout C.h + D x, and the gate's fixed factor
+    SiLU(z) all are.  A slip that adds a constant or mixes x into the decay breaks this."""
+    pr = _random_problem(80, T=7)
+    q = _random_problem(81, T=7)
+    al, be = 0.7, -1.3
+    kw = dict(D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    h1, y1 = path(pr, pr["h0"], **kw)
+    pr2 = dict(pr, x=q["x"])
+    h2, y2 = path(pr2, q["h0"], **kw)
+    pr3 = dict(pr, x=al * pr["x"] + be * q["x"])
+    h3, y3 = path(pr3, al * pr["h0"] + be * q["h0"], **kw)
+    np.testing.assert_allclose(h3, al * h1 + be * h2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y3, al * y1 + be * y2, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("path", [_run_decode_path, _run_prefill_path, _run_chunked_path])
+def test_scaling_B_up_and_C_down_leaves_outputs(path):
+    """From a zero state, h is proportional to B and y depends on B and C only through C.h:
+    B -> s B, C -> C / s scales h by s and leaves y unchanged.  Using C where B belongs (or the
+    reverse) anywhere breaks it."""
+    pr = _random_problem(82, T=7)
+    s = 3.0
+    kw = dict(D=pr["D"], dt_bias=pr["dt_bias"], z=pr["z"])
+    zero = np.zeros_like(pr["h0"])
+    h1, y1 = path(pr, zero, **kw)
+    h2, y2 = path(dict(pr, B=s * pr["B"], C=pr["C"] / s), zero, **kw)
+    np.testing.assert_allclose(h2, s * h1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y2, y1, rtol=1e-12, atol=1e-12)
