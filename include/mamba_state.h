@@ -28,10 +28,13 @@
  *    and never synchronise the host.
  *  - Errors the host can see (null required pointer, unsupported shape or dtype, a pointer
  *    not 16-byte aligned, a launch failure) return a negative mamba_status and launch
- *    nothing.  Errors that depend on device data (a slot id outside the pool, an accept
- *    length out of range, bad cu_seqlens) are found in the kernel: the affected unit is
- *    left untouched and a MAMBA_ERR_* bit is OR-ed into *err_word (a device int32 the
- *    caller zeroes and reads; it may be NULL to ignore such errors).
+ *    nothing.  Errors that depend on device data (a slot id outside the pool, i.e. below -1
+ *    or >= num_slots, an accept length out of range, bad cu_seqlens) are found in the kernel:
+ *    the affected unit is left untouched and a MAMBA_ERR_* bit is OR-ed into *err_word (a
+ *    device int32 the caller zeroes and reads; it may be NULL to ignore such errors).  A
+ *    bounded wait that gives up (MAMBA_ERR_TIMEOUT) is the one exception: see that bit.
+ *  - The method's domain is A <= 0 and steps Delta >= 0 (Delta = softplus(.) > 0 with
+ *    dt_softplus): every decay factor exp(Delta*A) is then at most 1, for any step size.
  *  - Slot ids within one call must be distinct (also across slot_ids and scratch_slots);
  *    the result is undefined otherwise.  Slot id -1 marks a padding row: its state and its
  *    output rows are not touched.
@@ -60,11 +63,15 @@ typedef enum {
 typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
 
 /* Data-dependent error bits OR-ed into *err_word. */
-#define MAMBA_ERR_SLOT_RANGE 0x1   /* a slot / scratch / checkpoint slot id outside [0, num_slots) */
+#define MAMBA_ERR_SLOT_RANGE 0x1   /* a slot / scratch / checkpoint slot id below -1 or >= num_slots
+                                      (-1 is padding / skip wherever a call allows it) */
 #define MAMBA_ERR_ACCEPT_RANGE 0x2 /* an accept length outside [0, ntok] */
 #define MAMBA_ERR_SEQLENS 0x4      /* cu_seqlens not non-decreasing from 0 to total_tokens */
 #define MAMBA_ERR_TIMEOUT 0x8      /* an asynchronous copy or matrix operation did not complete within the
-                                      kernel's bounded wait; that row / sequence is incomplete */
+                                      kernel's bounded wait; that row / sequence is incomplete: its
+                                      output is not written and its state may be partly advanced
+                                      (some heads updated, others not), so restore it from a
+                                      checkpoint or a copy before using it again */
 
 /* One Mamba2 layer [P1 state shapes, P4 block equations]. */
 typedef struct mamba_layer_desc {
@@ -282,7 +289,7 @@ size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *desc, int32_t to
  *   ckpt_slots       (nseq, max_ckpt) int32 or NULL;  ckpt_interval must be a positive
  *                    multiple of chunk when given.
  *   chunk            tokens per chunk; 256 is compiled.
- *   x                (total_tokens, nheads, head_dim) act_dtype (bf16 only).
+ *   x                (total_tokens, nheads, head_dim) act_dtype.
  *   dt               (total_tokens, nheads) dt_dtype.
  *   A (nheads) fp32;  D, dt_bias (nheads) fp32 or NULL.
  *   B, C             (total_tokens, n_groups, d_state) act_dtype.
@@ -290,6 +297,12 @@ size_t mamba_chunk_scan_workspace_bytes(const mamba_layer_desc *desc, int32_t to
  *   y                (total_tokens, nheads, head_dim) act_dtype.
  *   workspace        device buffer of at least mamba_chunk_scan_workspace_bytes(...) bytes,
  *                    16-byte aligned (MAMBA_ENOSPACE when workspace_bytes is smaller).
+ * Paths: bf16 activations with a bf16 state pool at head_dim 64, d_state 128 and a chunk that
+ * is a multiple of 128 run on the tensor cores (bf16 matrix operands, fp32 accumulation and
+ * state).  Every other case, and any fp32 state pool, runs in fp32 on the CUDA cores, which
+ * requires chunk 256, head_dim <= 64, and d_state a power of two in 32..256 with
+ * 256 / d_state dividing head_dim (MAMBA_EUNSUPPORTED otherwise): an fp32 pool's states are
+ * computed and written in fp32 throughout.
  */
 int mamba_chunk_scan(const mamba_layer_desc *desc, void *ssm_pool, int64_t ssm_slot_stride,
                      int64_t num_slots, const int32_t *cu_seqlens, int32_t nseq,

@@ -12,7 +12,12 @@
 //     h     = exp(cum_end) h_prev + S                     (state passing across chunks)
 //
 // This file is the portable CUDA-core form: six launches that communicate through a
-// caller-provided workspace (chunk table, Delta and cum, G per group, per-chunk states).
+// caller-provided workspace (chunk table, Delta and cum, G per group, per-chunk states).  It is
+// the fp32 path (fp32 activations, any fp32 state pool), so the cumulative sums are kept in
+// fp64: with large steps |cum| grows to hundreds within a chunk, and a decay exponent formed as
+// the difference of two fp32 sums of that size would carry an absolute error of ~1e-4.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -41,7 +46,7 @@ static ScanLayout scan_layout(int T, int nseq, int Q, int H, int G, int P, int N
     L.off_dl = off;
     off = round_up(off + sizeof(float) * (size_t)L.nchunks_max * H * Q, 256);
     L.off_cum = off;
-    off = round_up(off + sizeof(float) * (size_t)L.nchunks_max * H * Q, 256);
+    off = round_up(off + sizeof(double) * (size_t)L.nchunks_max * H * Q, 256);
     L.off_cb = off;
     off = round_up(off + sizeof(float) * (size_t)L.nchunks_max * G * Q * Q, 256);
     L.off_states = off;
@@ -79,7 +84,9 @@ struct ScanArgs {
     int32_t *err;
     int nchunks_max;
     int32_t *meta;
-    float *dl, *cum, *cb, *states;
+    float *dl;
+    double *cum;
+    float *cb, *states;
 };
 
 // ---------------------------------------------------------------------------------------
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(1024) k_chunk_prep(const ScanArgs a) {
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int c = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
     if (c >= *tb.count) return;
-    extern __shared__ float sc[];
+    extern __shared__ double sc[];
     const int len = tb.len[c];
     float delta = 0.0f;
     if (t < len) {
@@ -135,10 +142,10 @@ __global__ void __launch_bounds__(1024) k_chunk_prep(const ScanArgs a) {
                         (a.dt_bias ? a.dt_bias[h] : 0.0f);
         delta = a.dt_softplus ? softplus_f(s) : s;
     }
-    sc[t] = t < len ? delta * a.A[h] : 0.0f;
+    sc[t] = t < len ? (double)delta * (double)a.A[h] : 0.0;
     __syncthreads();
     for (int off = 1; off < blockDim.x; off <<= 1) {  // inclusive scan
-        const float v = t >= off ? sc[t - off] : 0.0f;
+        const double v = t >= off ? sc[t - off] : 0.0;
         __syncthreads();
         sc[t] += v;
         __syncthreads();
@@ -205,9 +212,9 @@ __global__ void __launch_bounds__(256) k_chunk_state(const ScanArgs a) {
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= *tb.count) return;
     const int len = tb.len[c], g = h / a.HG, P = a.P, N = a.N;
-    const float *cum = a.cum + ((int64_t)c * a.H + h) * a.Q;
+    const double *cum = a.cum + ((int64_t)c * a.H + h) * a.Q;
     const float *dl = a.dl + ((int64_t)c * a.H + h) * a.Q;
-    const float cum_end = cum[len - 1];
+    const double cum_end = cum[len - 1];
     extern __shared__ float sm[];
     float *Xs = sm;            // [32][P]  weighted x
     float *Bs = sm + 32 * P;   // [32][N]
@@ -224,7 +231,8 @@ __global__ void __launch_bounds__(256) k_chunk_state(const ScanArgs a) {
             const int r = e / P, p = e % P, j = j0 + r;
             float v = 0.0f;
             if (j < len)
-                v = expf(cum_end - cum[j]) * dl[j] * to_f32(xg[((int64_t)(tb.start[c] + j) * a.H + h) * P + p]);
+                v = expf((float)(cum_end - cum[j])) * dl[j] *
+                    to_f32(xg[((int64_t)(tb.start[c] + j) * a.H + h) * P + p]);
             Xs[e] = v;
         }
         for (int e = tid; e < 32 * N; e += 256) {
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(256) k_state_pass(const ScanArgs a) {
         float *S = a.states + ((int64_t)c * a.H + h) * PN + e;
         const float Sv = *S;
         *S = hv;  // state before chunk c
-        const float decay = expf(a.cum[((int64_t)c * a.H + h) * a.Q + len - 1]);
+        const float decay = expf((float)a.cum[((int64_t)c * a.H + h) * a.Q + len - 1]);
         hv = fmaf(decay, hv, Sv);
         if (a.ckpt_slots && a.ckpt_interval > 0) {
             const int done = tb.kidx[c] * a.Q + len;
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
     const int len = tb.len[c], i0 = ti * 64;
     if (i0 >= len) return;
     const int g = h / a.HG, P = a.P, N = a.N, Q = a.Q;
-    const float *cum = a.cum + ((int64_t)c * a.H + h) * Q;
+    const double *cum = a.cum + ((int64_t)c * a.H + h) * Q;
     const float *dl = a.dl + ((int64_t)c * a.H + h) * Q;
     const float *G = a.cb + ((int64_t)c * a.G + g) * Q * Q;
     const ActT *xg = static_cast<const ActT *>(a.x);
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
         for (int e = tid; e < 64 * 32; e += 256) {
             const int r = e / 32, k = e % 32, i = i0 + r, j = j0 + k;
             float v = 0.0f;
-            if (i < len && j < len && j <= i) v = G[(int64_t)i * Q + j] * expf(cum[i] - cum[j]) * dl[j];
+            if (i < len && j < len && j <= i) v = G[(int64_t)i * Q + j] * expf((float)(cum[i] - cum[j])) * dl[j];
             Ms[r][k] = v;
         }
         for (int e = tid; e < 32 * 64; e += 256) {
@@ -375,7 +383,7 @@ __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
     for (int u = 0; u < 4; ++u) {
         const int i = i0 + ty * 4 + u;
         if (i >= len) continue;
-        const float dec = expf(cum[i]);
+        const float dec = expf((float)cum[i]);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const int p = tx * 4 + v;
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
 template <typename ActT, typename StateT>
 static int launch_scan(const ScanArgs &a, cudaStream_t st) {
     k_chunk_meta<<<1, 32, 0, st>>>(a);
-    k_chunk_prep<<<dim3(a.nchunks_max, a.H), a.Q, sizeof(float) * a.Q, st>>>(a);
+    k_chunk_prep<<<dim3(a.nchunks_max, a.H), a.Q, sizeof(double) * a.Q, st>>>(a);
     k_chunk_cb<ActT><<<dim3(a.nchunks_max, a.G, 16), 256, 0, st>>>(a);
     const size_t smem_state = sizeof(float) * 32 * (size_t)(a.P + a.N);
     k_chunk_state<ActT><<<dim3(a.nchunks_max, a.H), 256, smem_state, st>>>(a);
@@ -416,7 +424,7 @@ static int scan_shape_ok(const mamba_layer_desc *d, int chunk) {
     return MAMBA_OK;
 }
 
-// The tensor-core path (bf16 activations, head_dim 64, d_state 128): returns a status, or 1 when
+// The tensor-core path (bf16 activations and state, head_dim 64, d_state 128): returns a status, or 1 when
 // the layer is not eligible and the portable path must run.
 static int try_scan_tc(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride, int64_t num_slots,
                        const int32_t *cu_seqlens, int32_t nseq, int32_t total_tokens, const int32_t *slot_ids,
@@ -483,7 +491,7 @@ extern "C" int mamba_chunk_scan(const mamba_layer_desc *d, void *ssm_pool, int64
     char *ws = static_cast<char *>(workspace);
     a.meta = reinterpret_cast<int32_t *>(ws + L.off_meta);
     a.dl = reinterpret_cast<float *>(ws + L.off_dl);
-    a.cum = reinterpret_cast<float *>(ws + L.off_cum);
+    a.cum = reinterpret_cast<double *>(ws + L.off_cum);
     a.cb = reinterpret_cast<float *>(ws + L.off_cb);
     a.states = reinterpret_cast<float *>(ws + L.off_states);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -511,24 +519,42 @@ extern "C" int mamba_chunk_scan(const mamba_layer_desc *d, void *ssm_pool, int64
 
 static __device__ __align__(256) unsigned char g_scan_scratch[MS_STATIC_SCAN_SCRATCH_BYTES];
 
-// Per-device address of g_scan_scratch, looked up once per device (with that device current).
+// The driver's cuCtxGetCurrent, looked up once (no allocation).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+static CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
+
+// Device address of g_scan_scratch for the current device, looked up with that device current on
+// the first call and again whenever the device's context has changed since (after a
+// cudaDeviceReset the module, and with it the array, is loaded anew at another address).
 static void *static_scratch_address(int *status) {
     constexpr int kMaxDevices = 64;
     static void *addr[kMaxDevices] = {};
+    static CUcontext ctx_of[kMaxDevices] = {};
     static std::mutex mu;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        *status = MAMBA_ECUDA;
-        return nullptr;
-    }
+    *status = MAMBA_ECUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (cudaSetDevice(dev) != cudaSuccess) return nullptr;  // same device: makes its primary context current
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx_of[dev] != ctx) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess || !p) {
-            *status = MAMBA_ECUDA;
-            return nullptr;
-        }
+        if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess || !p) return nullptr;
         addr[dev] = p;
+        ctx_of[dev] = ctx;
     }
     *status = MAMBA_OK;
     return addr[dev];
@@ -579,7 +605,7 @@ extern "C" int mamba_chunk_scan_noalloc(const mamba_layer_desc *d, void *ssm_poo
     char *ws = static_cast<char *>(workspace);
     a.meta = reinterpret_cast<int32_t *>(ws + L.off_meta);
     a.dl = reinterpret_cast<float *>(ws + L.off_dl);
-    a.cum = reinterpret_cast<float *>(ws + L.off_cum);
+    a.cum = reinterpret_cast<double *>(ws + L.off_cum);
     a.cb = reinterpret_cast<float *>(ws + L.off_cb);
     a.states = reinterpret_cast<float *>(ws + L.off_states);
     cudaStream_t st = static_cast<cudaStream_t>(stream);

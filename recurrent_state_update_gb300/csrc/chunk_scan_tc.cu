@@ -36,6 +36,7 @@ constexpr int TN = 128;  // d_state
 constexpr uint32_t BLK = 16384;  // one 128-row x 128-byte swizzled block
 constexpr uint32_t kPolls = umma::kWaitPolls;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float kDiagSpan = 96.0f;  // largest base-2 exponent span of a diagonal block taken factored
 
 // shared-memory map (from a 1024-aligned base)
 constexpr uint32_t OFF_B = 0;          // B tile, rows j: [n 0..63 | n 64..127]
@@ -52,7 +53,8 @@ struct Small {
     float cum2[SQ];   // cum * log2(e)
     float delta[SQ];
     float w[SQ];
-    float ecol[SQ];  // column factors of the masked G
+    float ecol[SQ];   // column factors of the masked G below the diagonal blocks
+    float ecold[SQ];  // column factors inside a diagonal block
     float warp_tot[4];
 };
 static_assert(sizeof(Small) <= 4096, "small area");
@@ -267,12 +269,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         const float cend = sv->cum2[L - 1];
         if (tid < SQ) {
             // w_j = exp(cum_end - cum_j) Delta_j for the chunk state, and the column factor of the
-            // masked G: e_j = exp(cum_ref - cum_j) Delta_j with cum_ref the first column of j's
-            // 32-column block (exp(cum_i - cum_j) = exp(cum_i - cum_ref) e_j / Delta_j, both factors
-            // bounded for i >= j)
+            // masked G below the diagonal blocks: e_j = exp(cum_ref - cum_j) Delta_j with cum_ref the
+            // cumulative sum at the LAST column of j's 32-column block.  For a row i past that block,
+            // exp(cum_i - cum_j) = exp(cum_i - cum_ref) exp(cum_ref - cum_j) with both exponents <= 0
+            // (cum is non-increasing: Delta >= 0, A <= 0), so neither factor can overflow whatever
+            // the step size; a factor that underflows stands for a product below fp32's range.
+            // Inside a diagonal block the same factoring with the block's FIRST column as the reference
+            // (e_j = exp(cum_first - cum_j) Delta_j >= Delta_j, row factor <= 1) is used only when the
+            // block spans at most 96 in base-2 exponent, so that both factors stay within 2^+-96;
+            // a block with larger steps forms each decay from its own difference.
             const float cj = sv->cum2[tid];
             sv->w[tid] = tid < L ? exp2f(cend - cj) * dlt : 0.0f;
-            sv->ecol[tid] = tid < L ? exp2f(sv->cum2[tid & ~31] - cj) * dlt : 0.0f;
+            sv->ecol[tid] = tid < L ? exp2f(sv->cum2[tid | 31] - cj) * dlt : 0.0f;
+            sv->ecold[tid] = tid < L ? exp2f(fminf(sv->cum2[tid & ~31] - cj, kDiagSpan)) * dlt : 0.0f;
         }
         // this thread's 32 columns of its token row of X (for D x), read before the tile is scaled
         uint4 xrow[4];
@@ -295,17 +304,31 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
                 if (jb <= q) {  // warp-uniform: block jb can hold columns j <= i for these rows
                     float gv[32];
                     tmem_ld32(t_g + lane_base + jb * 32, gv);
-                    const float rf = row < L ? exp2f(ci - sv->cum2[jb * 32]) : 0.0f;
-                    const float *ec = sv->ecol + jb * 32;
-                    if (jb < q) {
+                    if (jb < q) {  // every row is past the block: the factored form above
+                        const float rf = row < L ? exp2f(ci - sv->cum2[jb * 32 + 31]) : 0.0f;
+                        const float *ec = sv->ecol + jb * 32;
 #pragma unroll
                         for (int qq = 0; qq < 32; qq += 2)
                             pk[qq / 2] = pack_bf16x2(gv[qq] * rf * ec[qq], gv[qq + 1] * rf * ec[qq + 1]);
-                    } else {  // diagonal block: j <= i
+                    } else if (sv->cum2[jb * 32] - sv->cum2[jb * 32 + 31] <= kDiagSpan) {
+                        // diagonal block, j <= i, span within 2^96: factored at the block's first column
+                        const float rf = row < L ? exp2f(ci - sv->cum2[jb * 32]) : 0.0f;
+                        const float *ec = sv->ecold + jb * 32;
 #pragma unroll
                         for (int qq = 0; qq < 32; qq += 2)
                             pk[qq / 2] = pack_bf16x2(qq <= lane ? gv[qq] * rf * ec[qq] : 0.0f,
                                                      qq + 1 <= lane ? gv[qq + 1] * rf * ec[qq + 1] : 0.0f);
+                    } else {  // diagonal block with large steps: each decay from its own difference (<= 0)
+                        const float *cc = sv->cum2 + jb * 32;
+                        const float *dd = sv->delta + jb * 32;
+                        const bool live = row < L;
+#pragma unroll
+                        for (int qq = 0; qq < 32; qq += 2) {
+                            const float m0 = live && qq <= lane ? gv[qq] * exp2f(ci - cc[qq]) * dd[qq] : 0.0f;
+                            const float m1 =
+                                live && qq + 1 <= lane ? gv[qq + 1] * exp2f(ci - cc[qq + 1]) * dd[qq + 1] : 0.0f;
+                            pk[qq / 2] = pack_bf16x2(m0, m1);
+                        }
                     }
                 } else {
 #pragma unroll
@@ -507,7 +530,10 @@ static bool make_map(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t ro
 }
 
 bool scan_tc_eligible(const mamba_layer_desc *d, int chunk) {
-    return d->act_dtype == MAMBA_BF16 && d->head_dim == TP && d->d_state == TN && chunk > 0 && chunk % SQ == 0;
+    // an fp32 state pool asks for fp32 state arithmetic: its bf16 operand copies (M, w X, h) would
+    // bound the written state at bf16 precision, so it takes the fp32 CUDA-core path instead
+    return d->act_dtype == MAMBA_BF16 && d->state_dtype == MAMBA_BF16 && d->head_dim == TP && d->d_state == TN &&
+           chunk > 0 && chunk % SQ == 0;
 }
 
 size_t scan_tc_workspace_bytes(int nseq) { return ((size_t)(4 + nseq) * sizeof(int32_t) + 255) / 256 * 256; }

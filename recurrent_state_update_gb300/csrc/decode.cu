@@ -407,8 +407,8 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
 
     const int32_t s = a.slot[i];
-    if (s < 0) return;  // padding row
-    bool bad = s >= a.num_slots;
+    if (s == -1) return;  // padding row
+    bool bad = s < -1 || s >= a.num_slots;
     if (a.scratch)
         for (int j = 0; j < ntok; ++j) {
             const int32_t d = a.scratch[(int64_t)i * ntok + j];
@@ -839,7 +839,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
             int t = 0;
             for (int w = blockIdx.x; w < W && !*abort_flag; w += gridDim.x) {
                 const int32_t s = a.slot[w / G];
-                if (s >= a.num_slots && w % G == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+                if ((s < -1 || s >= a.num_slots) && w % G == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
                 if (s < 0 || s >= a.num_slots) continue;
                 const StateT *grp = pool + (int64_t)s * a.ssm_stride + (int64_t)(w % G) * HG * P * N;
                 for (int hl = 0; hl < HG; ++hl, ++t) {
@@ -860,7 +860,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
         const size_t xseg = (size_t)HG * P, bseg = N;  // channels per segment: x | B | C
         auto next_valid = [&](int w) {
             while (w < W && item_slot(w) < 0) {
-                if (ct == 0 && w % G == 0 && a.slot[w / G] >= a.num_slots) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+                if (ct == 0 && w % G == 0 && (a.slot[w / G] < -1 || a.slot[w / G] >= a.num_slots))
+                    flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
                 w += gridDim.x;
             }
             return w;
@@ -1115,8 +1116,8 @@ __global__ void __launch_bounds__(kConvThreads) k_conv_step(const ConvArgs a, in
         const int i = i0 + r;
         if (i >= batch) continue;
         const int32_t s = a.slot[i];
-        if (s < 0) continue;
-        if (s >= a.num_slots) {
+        if (s == -1) continue;  // padding row
+        if (s < -1 || s >= a.num_slots) {
             if (c0 == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
             continue;
         }
@@ -1189,8 +1190,8 @@ template <typename ActT>
 __global__ void __launch_bounds__(256) k_conv_update(const ConvArgs a) {
     const int cb = blockIdx.x, i = blockIdx.y, ntok = a.ntok;
     const int32_t s = a.slot[i];
-    if (s < 0) return;
-    if (s >= a.num_slots) {
+    if (s == -1) return;  // padding row
+    if (s < -1 || s >= a.num_slots) {
         if (threadIdx.x == 0 && cb == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
         return;
     }
@@ -1237,7 +1238,11 @@ template <typename ActT>
 __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
     const int unit = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
     const int32_t s = a.slot[i];
-    if (s < 0) return;
+    if (s == -1) return;  // padding row
+    if (s < -1) {
+        if (unit == 0 && tid == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
+        return;
+    }
     const int32_t acc = a.accept[i];
     if (acc < 0 || acc > a.ntok) {
         if (unit == 0 && tid == 0) flag_error(a.err, MAMBA_ERR_ACCEPT_RANGE);

@@ -61,7 +61,6 @@ __device__ __forceinline__ void store_row(StateT *p, const float (&h)[N]) {
     }
 }
 
-// Everything one row of one channel reads: its state, x, dt and z (slot < 0: nothing to do).
 // 2^x by the PTX approximate base-2 exponential (about 2 ulp); the decay arguments Delta A log2 e
 // are never positive, and very negative ones give 0, the limit.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -70,6 +69,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Everything one row of one channel reads: its state, x, dt and z (slot < 0: nothing to do).
 template <int N>
 struct M1Row {
     float h[N];
@@ -82,8 +82,8 @@ __device__ __forceinline__ void m1_load(const M1Args &a, int i, int d, M1Row<N> 
     r.slot = -1;
     if (i >= a.batch) return;
     const int32_t s = a.slot[i];
-    if (s < 0) return;  // padding row: nothing read or written
-    if (s >= a.num_slots) {
+    if (s == -1) return;  // padding row: nothing read or written
+    if (s < -1 || s >= a.num_slots) {
         if (d == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
         return;
     }
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kM1StreamThreads, 2) k_mamba1_stream(const M1S
                 }
                 unsigned char *sp = m1_smem + (size_t)st * L.bytes;
                 int32_t s = a.slot[i];
-                if (s >= a.num_slots) {
+                if (s < -1 || s >= a.num_slots) {
                     if (cb == 0) flag_error(a.err, MAMBA_ERR_SLOT_RANGE);
                     s = -1;
                 }

@@ -24,8 +24,8 @@ struct ScanTcParams {
     int32_t *meta;  // workspace: [valid, pad x3, order[nseq]]
 };
 
-// True when the tensor-core path handles this layer and chunk (bf16 activations, head_dim 64,
-// d_state 128, chunk a multiple of 128).
+// True when the tensor-core path handles this layer and chunk (bf16 activations and state,
+// head_dim 64, d_state 128, chunk a multiple of 128).
 bool scan_tc_eligible(const mamba_layer_desc *d, int chunk);
 
 // Workspace bytes of the tensor-core path.

@@ -16,6 +16,11 @@ Value distributions (the workload recipe):
   size stays in [1e-3, 0.1].
 Values are drawn in float64 and rounded once to the storage type (bf16 round-to-nearest-even
 or fp32); both the GPU and the oracle receive exactly those stored values.
+
+Wide-step inputs (parity cases beyond the configs' small steps; the method is defined for any
+step Delta > 0 and any A < 0): the step itself is drawn log-uniform in [lo, hi] per (token, head)
+and raw dt = softplus^-1(step) - dt_bias, so that with A down to -16 the per-token decay exponent
+Delta*|A| spans about 1e-3 .. 80 (WIDE_STEPS), or lies only in the large range (LARGE_STEPS).
 """
 from __future__ import annotations
 
@@ -127,6 +132,8 @@ def upcast(stored: np.ndarray, dtype: str) -> np.ndarray:
 # --------------------------------------------------------------------------------------
 
 DELTA_LO, DELTA_HI = 1e-3, 0.1
+WIDE_STEPS = (1e-3, 5.0)   # tiny and large steps mixed
+LARGE_STEPS = (0.2, 5.0)   # large steps only
 
 
 def _inv_softplus(u):
@@ -157,6 +164,18 @@ def raw_dt(g: np.random.Generator, dt_bias: np.ndarray, lead: tuple) -> np.ndarr
     return out
 
 
+def wide_dt(g: np.random.Generator, dt_bias: np.ndarray, lead: tuple, steps: tuple) -> np.ndarray:
+    """Raw dt per (lead..., head) whose step softplus(dt + dt_bias) is log-uniform in steps = (lo, hi)."""
+    lo, hi = steps
+    u = np.exp(g.uniform(math.log(lo), math.log(hi), size=lead + dt_bias.shape))
+    return _inv_softplus(u) - dt_bias.astype(np.float64)
+
+
+def step_dt(g: np.random.Generator, dt_bias: np.ndarray, lead: tuple, steps) -> np.ndarray:
+    """The configs' raw dt (steps None) or wide-step raw dt (steps = (lo, hi))."""
+    return raw_dt(g, dt_bias, lead) if steps is None else wide_dt(g, dt_bias, lead, steps)
+
+
 def xbc_values(g: np.random.Generator, shape: LayerShape, lead: tuple) -> np.ndarray:
     """Raw xBC rows (lead..., conv_dim): x channels N(0,1), B and C channels N(0,1)/sqrt(N)."""
     HP = shape.nheads * shape.head_dim
@@ -166,10 +185,10 @@ def xbc_values(g: np.random.Generator, shape: LayerShape, lead: tuple) -> np.nda
 
 
 def decode_inputs(g: np.random.Generator, shape: LayerShape, params: dict, batch: int, ntok: int,
-                  act: str, with_z: bool = True) -> dict:
+                  act: str, with_z: bool = True, steps=None) -> dict:
     """One decode step's inputs: xbc (batch, ntok, conv_dim), dt fp32 (batch, ntok, H), z."""
     xbc = store(xbc_values(g, shape, (batch, ntok)), act)
-    dt = store(raw_dt(g, params["dt_bias"], (batch, ntok)), F32)
+    dt = store(step_dt(g, params["dt_bias"], (batch, ntok), steps), F32)
     z = store(g.standard_normal((batch, ntok, shape.nheads * shape.head_dim)), act) if with_z else None
     return dict(xbc=xbc, dt=dt, z=z)
 
@@ -208,13 +227,13 @@ def cu_seqlens(lengths) -> np.ndarray:
 
 
 def prefill_inputs(g: np.random.Generator, shape: LayerShape, params: dict, T: int, act: str,
-                   dt_dtype: str = F32, with_z: bool = False) -> dict:
+                   dt_dtype: str = F32, with_z: bool = False, steps=None) -> dict:
     """Post-conv prefill inputs: x (T, H, P), B, C (T, G, N), dt (T, H), z (T, H, P) optional."""
     H, P, N, G = shape.nheads, shape.head_dim, shape.d_state, shape.n_groups
     x = store(g.standard_normal((T, H, P)), act)
     B = store(g.standard_normal((T, G, N)) / math.sqrt(N), act)
     C = store(g.standard_normal((T, G, N)) / math.sqrt(N), act)
-    dt = store(raw_dt(g, params["dt_bias"], (T,)), dt_dtype)
+    dt = store(step_dt(g, params["dt_bias"], (T,), steps), dt_dtype)
     z = store(g.standard_normal((T, H, P)), act) if with_z else None
     return dict(x=x, B=B, C=C, dt=dt, z=z)
 

@@ -183,7 +183,10 @@ def test_conv_varlen_full_size_sampled_channels():
 
 def test_prefill_conv_then_scan_matches_oracle_pipeline():
     """Prompt -> mamba_conv_varlen -> mamba_chunk_scan equals the oracle's conv followed by its
-    step recurrence (the whole prefill of a Mamba2 layer before the output projection)."""
+    step recurrence (the whole prefill of a Mamba2 layer before the output projection), within
+    the prefill bound 2e-2 per (64-token block, head) tile of y and per (slot, head) tile of the
+    state; the scan alone is also held to that bound against the oracle recurrence run on the
+    GPU's own conv outputs (which may differ from the oracle's rounded conv by one bf16 ulp)."""
     import torch
     shape = wl.LayerShape(nheads=4, head_dim=64, d_state=128, n_groups=2, conv_kernel=4)
     lengths = [300, 5, 129]
@@ -217,7 +220,20 @@ def test_prefill_conv_then_scan_matches_oracle_pipeline():
                                      post[:, HP + GN:].reshape(T, G, N), h0=h0, D=wl.upcast(prm["D"], wl.F32),
                                      dt_bias=wl.upcast(prm["dt_bias"], wl.F32))
     from gpu_util import tile_rel_err
-    assert tile_rel_err(f64(y).reshape(T, H, P).transpose(1, 0, 2), yr.transpose(1, 0, 2), 2) < 3e-2
-    got_h = f64(ssm)
+
+    def y_tiles(a):  # (T, H, P) -> (64-token block, head) tiles
+        a = np.concatenate([a, np.zeros(((-T) % 64, H, P))])
+        return a.reshape(-1, 64, H, P).transpose(0, 2, 1, 3)
+
+    got_y, got_h = f64(y).reshape(T, H, P), f64(ssm)
+    assert tile_rel_err(y_tiles(got_y), y_tiles(yr), 2) < 2e-2
     for s, sl in enumerate(pr.slot):
-        assert tile_rel_err(got_h[sl], hf[s], 2) < 3e-2
+        assert tile_rel_err(got_h[sl], hf[s], 2) < 2e-2
+    # the scan on exactly the inputs it received
+    ys, hs, _ = oracle.prefill_steps(pr.cu, f64(pr.x).reshape(T, H, P), wl.upcast(dt, wl.F32),
+                                     wl.upcast(prm["A"], wl.F32), f64(pr.B).reshape(T, G, N),
+                                     f64(pr.C).reshape(T, G, N), h0=h0, D=wl.upcast(prm["D"], wl.F32),
+                                     dt_bias=wl.upcast(prm["dt_bias"], wl.F32))
+    assert tile_rel_err(y_tiles(got_y), y_tiles(ys), 2) < 2e-2
+    for s, sl in enumerate(pr.slot):
+        assert tile_rel_err(got_h[sl], hs[s], 2) < 2e-2

@@ -2,8 +2,12 @@
 
 Tolerances (relative error per tile: (slot, head) for states, (row, head) for outputs):
   fp32 state: max error 1e-4;  bf16 state: max error 2e-2 per step (the oracle is fed the GPU's own
-  bf16 state from before the step); drift after 64 independent steps (oracle chain kept in fp64):
-  RMS error 3e-2, and max error under 64 * 2^-9, the bound for 64 round-to-nearest bf16 stores.
+  bf16 state from before the step); drift after 64 independent steps: y within 3e-2 (max) of the
+  fp64 oracle chain; the state within 3e-2 (max) of an oracle chain that stores its state in bf16
+  after every step as the pool does, and within 3e-2 RMS of the fp64 chain.  The state's max
+  error against the fp64 chain is not held to 3e-2: the test measures that bf16 storage alone
+  (the oracle's own bf16 chain) already drifts further than that, and holds the GPU to within
+  1.5x of the format's own drift.
 Slot indexing, padding and every byte the call must not touch are compared exactly.
 """
 import numpy as np
@@ -42,8 +46,8 @@ class Layer:
         self.act = act
 
 
-def _step_inputs(layer, seed, step, batch, ntok=1, with_z=True):
-    inp = wl.decode_inputs(wl.rng(seed, 1, step), layer.shape, layer.prm, batch, ntok, layer.act, with_z)
+def _step_inputs(layer, seed, step, batch, ntok=1, with_z=True, steps=None):
+    inp = wl.decode_inputs(wl.rng(seed, 1, step), layer.shape, layer.prm, batch, ntok, layer.act, with_z, steps)
     dev = dict(xbc=to_dev(inp["xbc"], layer.act), dt=to_dev(inp["dt"], wl.F32), z=to_dev(inp["z"], layer.act))
     o = dict(xbc=wl.upcast(inp["xbc"], layer.act), dt=inp["dt"].astype(np.float64),
              z=None if inp["z"] is None else wl.upcast(inp["z"], layer.act))
@@ -169,12 +173,14 @@ def test_padding_sweep_16_steps(batch):
 def test_bf16_drift_64_steps():
     """64 steps with the GPU chain and two oracle chains run independently.
 
-    Against the oracle chain kept in fp64 throughout: each GPU step stores the state in bf16
-    (relative rounding <= 2^-9), so single elements drift from it like a random walk; the drift
-    bound applies to the RMS error per tile, and the max error stays under 64 * 2^-9.
-    Against the oracle chain that stores its state in bf16 after every step, as the pool does:
-    what is left is the kernel's own arithmetic (fp32 against fp64), held to the drift bound as
-    a max error per tile."""
+    Against the oracle chain kept in fp64 throughout: y is held to the drift bound as a max error
+    per tile.  Each GPU step stores the state in bf16 (relative rounding <= 2^-9), so single state
+    elements drift from the fp64 chain like a random walk.  The oracle chain that stores its state
+    in bf16 after every step, as the pool does, measures that drift of the storage format itself:
+    the test asserts it exceeds the 3e-2 bound (so the bound cannot be met by any kernel that
+    stores bf16), holds the GPU's state to the bound in RMS against the fp64 chain, to 1.5x the
+    format's own max drift, and to the bound as a max error against the bf16 chain (what is left
+    there is the kernel's fp32 arithmetic against fp64)."""
     import torch
     S, batch, seed = 16, 8, 30
     shape, ssm, conv = _nemotron_pools(S, seed)
@@ -196,12 +202,96 @@ def test_bf16_drift_64_steps():
     got_h = f64(ssm[sl])
     got_y = f64(y).reshape(batch, shape.nheads, -1)
     ref_y = y_o.reshape(batch, shape.nheads, -1)
+    format_drift = tile_rel_err(b_ssm[slot], o_ssm[slot], 2)  # bf16 storage alone, no kernel involved
+    assert format_drift > BF16_DRIFT_TOL
+    assert tile_rel_err(got_y, ref_y, 1) < BF16_DRIFT_TOL
     assert tile_rms_err(got_h, o_ssm[slot], 2) < BF16_DRIFT_TOL
-    assert tile_rms_err(got_y, ref_y, 1) < BF16_DRIFT_TOL
-    assert tile_rel_err(got_h, o_ssm[slot], 2) < 64 * 2.0 ** -9
-    assert tile_rel_err(got_y, ref_y, 1) < 64 * 2.0 ** -9
+    assert tile_rel_err(got_h, o_ssm[slot], 2) < 1.5 * format_drift
     assert tile_rel_err(got_h, b_ssm[slot], 2) < BF16_DRIFT_TOL
     assert tile_rel_err(got_y, y_b.reshape(batch, shape.nheads, -1), 1) < BF16_DRIFT_TOL
+
+
+@pytest.mark.parametrize("state,batch,ntok", [(wl.BF16, 64, 1), (wl.BF16, 4, 1), (wl.F32, 64, 1), (wl.BF16, 24, 4)])
+def test_decode_wide_steps(state, batch, ntok):
+    """Steps log-uniform in [1e-3, 5] (Delta*|A| up to ~80 per token) through each launch path: the
+    persistent stream (batch 64), the cluster split (batch 4) and several tokens into scratch
+    slots (4 tokens); three steps in a row, each against one oracle step from the GPU's state."""
+    import torch
+    S, seed = 2 * batch * (1 + ntok) + 8, 90 + batch + ntok
+    shape, ssm, conv = _nemotron_pools(S, seed, state, spec=ntok if ntok > 1 else 0)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape, state=state)
+    ids = wl.rng(seed, 3).choice(S, size=batch * (1 + (ntok if ntok > 1 else 0)), replace=False).astype(np.int32)
+    slot = ids[:batch]
+    scratch = ids[batch:].reshape(batch, ntok) if ntok > 1 else None
+    tol = BF16_STEP_TOL if state == wl.BF16 else FP32_TOL
+    for step in range(3):
+        o_ssm, o_conv = f64(ssm), f64(conv)
+        dev, o = _step_inputs(layer, seed, step, batch, ntok=ntok, steps=wl.WIDE_STEPS)
+        y = torch.empty(batch, ntok, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+        _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, scratch_t=None if scratch is None else to_i32(scratch))
+        torch.cuda.synchronize()
+        y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
+        got_y = f64(y)
+        assert np.isfinite(got_y).all()
+        assert tile_rel_err(got_y.reshape(batch, ntok, shape.nheads, -1),
+                            y_o.reshape(batch, ntok, shape.nheads, -1), 1) < 2e-2
+        targets = [slot] if scratch is None else [scratch[:, j] for j in range(ntok)]
+        for tg in targets:
+            got_h = f64(ssm[torch.from_numpy(tg.copy()).long().cuda()])
+            assert np.isfinite(got_h).all()
+            assert tile_rel_err(got_h, o_ssm[tg], 2) < tol
+        np.testing.assert_array_equal(f64(conv[torch.from_numpy(slot).long().cuda()]), o_conv[slot])
+
+
+@pytest.mark.parametrize("batch", [4, 64])
+def test_slot_ids_below_minus_one_are_flagged(batch):
+    """A slot id below -1 is outside the pool, not padding: the decode step, the standalone conv
+    update and the commit flag MAMBA_ERR_SLOT_RANGE and leave that row's state, conv window and
+    output untouched (batch 4 takes the cluster split, batch 64 the persistent stream)."""
+    import torch
+    S, seed = 2 * batch + 8, 110 + batch
+    shape, ssm, conv = _nemotron_pools(S, seed, spec=2)
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
+    slot[1] = -2
+    slot[batch - 1] = -7
+    ssm0, conv0 = ssm.clone(), conv.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev, _ = _step_inputs(layer, seed, 0, batch)
+    y = torch.zeros(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
+    assert bool((y[1] == 0).all()) and bool((y[batch - 1] == 0).all())
+    live = set(slot[slot >= 0].tolist())
+    for s in range(S):
+        if s not in live:
+            assert torch.equal(ssm[s], ssm0[s]) and torch.equal(conv[s], conv0[s])
+    # the standalone conv update
+    err.zero_()
+    conv1 = conv.clone()
+    out = torch.zeros(batch, 1, shape.conv_dim, device="cuda", dtype=torch.bfloat16)
+    bd.mamba_conv_update(desc, conv, to_i32(slot), dev["xbc"], layer.d["conv_w"], out, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
+    assert bool((out[1] == 0).all()) and bool((out[batch - 1] == 0).all())
+    for s in range(S):
+        if s not in live:
+            assert torch.equal(conv[s], conv1[s])
+    # the commit
+    err.zero_()
+    ssm2, conv2 = ssm.clone(), conv.clone()
+    scratch = np.full((batch, 1), 0, np.int32)
+    scratch[:, 0] = [s_ for s_ in range(S) if s_ not in live][:batch]
+    accept = np.ones(batch, np.int32)
+    bd.mamba_spec_commit(desc, ssm, to_i32(slot), to_i32(scratch), to_i32(accept), conv_pool=conv, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
+    for s in range(S):  # the flagged rows wrote nothing; the scratch slots are only read
+        if s not in live:
+            assert torch.equal(ssm[s], ssm2[s]) and torch.equal(conv[s], conv2[s])
 
 
 def test_permuted_slots_permute_results_bit_exactly():

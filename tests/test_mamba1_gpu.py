@@ -172,3 +172,22 @@ def test_mamba1_bad_slot_flagged():
     inp, before, y = m.step(err=err)
     assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
     assert np.isnan(y[1]).all()
+
+
+@pytest.mark.parametrize("Dn,N,state,batch", [(64, 16, wl.BF16, 3), (5120, 16, wl.BF16, 40), (64, 64, wl.F32, 5)])
+def test_mamba1_slot_below_minus_one_flagged(Dn, N, state, batch):
+    """A slot id below -1 is outside the pool, not padding: flagged, its row's output and every
+    slot no live row owns are left untouched (the bulk-copy stream for state rows of up to 64
+    bytes, the per-channel kernel for wider ones)."""
+    import torch
+    m = M1(Dn, N, batch + 4, batch, state, wl.BF16, seed=99 + batch)
+    m.slot[1] = -2
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    inp, before, y = m.step(err=err)
+    assert int(err.item()) & bd.MAMBA_ERR_SLOT_RANGE
+    assert np.isnan(y[1]).all()
+    after = f64(m.pool)
+    owned = set(int(s) for s in m.slot if s >= 0)
+    for s in range(after.shape[0]):
+        if s not in owned:
+            np.testing.assert_array_equal(after[s], before[s])
