@@ -806,6 +806,11 @@ def main():
                     help="time one form alone (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        # one process per GPU: N > 1 is launched by torch.distributed.run, which sets WORLD_SIZE
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 ranks with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -21,6 +21,9 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
               "--expt-relaxed-constexpr"]
+# NVTX ranges around every exported call are built in; MAMBA_NVTX=0 (with --force) leaves them out.
+if os.environ.get("MAMBA_NVTX", "1") == "0":
+    NVCC_FLAGS.append("-DMS_NVTX=0")
 
 
 def _nvcc() -> str:

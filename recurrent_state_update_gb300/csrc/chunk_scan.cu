@@ -463,6 +463,7 @@ extern "C" int mamba_chunk_scan(const mamba_layer_desc *d, void *ssm_pool, int64
                                 const void *x, const void *dt, const float *A, const void *B, const void *C,
                                 const float *D, const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
                                 void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_chunk_scan");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (nseq < 0 || total_tokens < 0 || chunk <= 0) return MAMBA_EINVAL;
@@ -570,6 +571,7 @@ extern "C" int mamba_chunk_scan_noalloc(const mamba_layer_desc *d, void *ssm_poo
                                         const void *dt, const float *A, const void *B, const void *C,
                                         const float *D, const float *dt_bias, int32_t dt_softplus, const void *z,
                                         void *y, int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_chunk_scan_noalloc");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (nseq < 0 || total_tokens < 0 || chunk <= 0) return MAMBA_EINVAL;

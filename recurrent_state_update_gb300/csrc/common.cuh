@@ -8,7 +8,31 @@
 
 #include "mamba_state.h"
 
+// NVTX ranges: every exported call that launches work opens a range named after the call for
+// its host-side duration (argument checks and launches), so a timeline tool (Nsight Systems,
+// or any NVTX injection library) shows which library call issued which kernels.  Built in by
+// default; compile with -DMS_NVTX=0 to leave them out.  With no tool attached a range costs a
+// call through a null-checked function pointer.
+#ifndef MS_NVTX
+#define MS_NVTX 1
+#endif
+#if MS_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace ms {
+
+#if MS_NVTX
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define MS_TRACE(name) ::ms::NvtxRange ms_nvtx_range_(name)
+#else
+#define MS_TRACE(name) ((void)0)
+#endif
 
 using bf16 = __nv_bfloat16;
 

@@ -379,6 +379,7 @@ extern "C" int mamba_conv_varlen(const mamba_layer_desc *d, void *conv_pool, int
                                  const int32_t *slot_ids, const uint8_t *has_initial_state, const void *xbc,
                                  const float *conv_w, const float *conv_b, void *x_out, void *B_out, void *C_out,
                                  int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_conv_varlen");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (nseq < 0 || total_tokens < 0) return MAMBA_EINVAL;

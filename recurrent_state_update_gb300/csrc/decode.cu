@@ -1503,6 +1503,7 @@ extern "C" int mamba_state_update(const mamba_layer_desc *d, void *ssm_pool, int
                                   const void *xbc, const void *dt, const float *A, const float *D,
                                   const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
                                   int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_state_update");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (batch < 0 || batch > 65535 || ntok < 1 || ntok > 8) return MAMBA_EINVAL;
@@ -1538,6 +1539,7 @@ extern "C" int mamba_conv_update(const mamba_layer_desc *d, void *conv_pool, int
                                  int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
                                  const void *xbc_in, const float *conv_w, const float *conv_b, void *xbc_out,
                                  int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_conv_update");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (batch < 0 || batch > 65535 || ntok < 1 || ntok > 64) return MAMBA_EINVAL;
@@ -1570,6 +1572,7 @@ extern "C" int mamba1_conv_update(const mamba1_layer_desc *d, void *conv_pool, i
                                   int64_t num_slots, const int32_t *slot_ids, int32_t batch, int32_t ntok,
                                   const void *x_in, const float *conv_w, const float *conv_b, void *x_out,
                                   int32_t *err_word, void *stream) {
+    MS_TRACE("mamba1_conv_update");
     if (!d || d->d_inner <= 0 || d->conv_kernel < 2 || d->conv_kernel > 8 || d->num_spec < 0 || d->num_spec > 32 ||
         !dtype_ok(d->act_dtype) || !dtype_ok(d->conv_dtype))
         return MAMBA_EINVAL;
@@ -1604,6 +1607,7 @@ extern "C" int mamba_spec_commit(const mamba_layer_desc *d, void *ssm_pool, int6
                                  const int32_t *slot_ids, const int32_t *scratch_slots,
                                  const int32_t *accept_len, int32_t batch, int32_t ntok, int32_t *err_word,
                                  void *stream) {
+    MS_TRACE("mamba_spec_commit");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (batch < 0 || batch > 65535 || ntok < 1) return MAMBA_EINVAL;

@@ -397,6 +397,7 @@ extern "C" int mamba1_state_update(const mamba1_layer_desc *d, void *ssm_pool, i
                                    const void *dt, const float *A, const void *B, const void *C, const float *D,
                                    const float *dt_bias, int32_t dt_softplus, const void *z, void *y,
                                    int32_t *err_word, void *stream) {
+    MS_TRACE("mamba1_state_update");
     if (!d || d->d_inner <= 0 || d->d_inner % 8 || !dtype_ok(d->state_dtype) || !dtype_ok(d->act_dtype) ||
         !dtype_ok(d->dt_dtype))
         return MAMBA_EINVAL;

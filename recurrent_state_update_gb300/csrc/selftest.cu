@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(32) k_wait_timeout(int32_t *err, uint64_t *ela
 using namespace ms;
 
 extern "C" int mamba_selftest_wait_timeout(int32_t *err_word, uint64_t *elapsed_ns, void *stream) {
+    MS_TRACE("mamba_selftest_wait_timeout");
     if (!err_word) return MAMBA_EINVAL;
     k_wait_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err_word, elapsed_ns);
     return launch_status();

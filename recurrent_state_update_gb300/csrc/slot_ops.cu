@@ -326,6 +326,7 @@ using namespace ms;
 extern "C" int mamba_slot_copy(const mamba_layer_desc *d, void *ssm_pool, int64_t ssm_slot_stride, int64_t num_slots,
                                void *conv_pool, int64_t conv_slot_stride, const int32_t *src_slots,
                                const int32_t *dst_slots, int32_t n, int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_slot_copy");
     int rc = check_desc(d);
     if (rc != MAMBA_OK) return rc;
     if (n < 0 || n > 65535) return MAMBA_EINVAL;
@@ -365,6 +366,7 @@ extern "C" int mamba_ckpt_store_int8(const mamba_layer_desc *d, const void *ssm_
                                      const void *conv_pool, int64_t conv_slot_stride, int64_t num_slots,
                                      const int32_t *src_slots, const int32_t *dst_entries, int32_t n, void *store,
                                      int64_t num_entries, int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_ckpt_store_int8");
     QArgs a;
     const int rc = q_args(d, ssm_pool, ssm_slot_stride, conv_pool, conv_slot_stride, num_slots, src_slots, dst_entries,
                           n, store, num_entries, err_word, a);
@@ -389,6 +391,7 @@ extern "C" int mamba_ckpt_load_int8(const mamba_layer_desc *d, void *ssm_pool, i
                                     void *conv_pool, int64_t conv_slot_stride, int64_t num_slots,
                                     const int32_t *src_entries, const int32_t *dst_slots, int32_t n, const void *store,
                                     int64_t num_entries, int32_t *err_word, void *stream) {
+    MS_TRACE("mamba_ckpt_load_int8");
     QArgs a;
     const int rc = q_args(d, ssm_pool, ssm_slot_stride, conv_pool, conv_slot_stride, num_slots, dst_slots, src_entries,
                           n, store, num_entries, err_word, a);

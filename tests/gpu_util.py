@@ -64,3 +64,35 @@ def tile_rms_err(got, ref, tile_axes):
     den = np.sqrt((ref ** 2).sum(axis=axes))
     den = np.where(den == 0, 1.0, den)
     return float((num / den).max())
+
+
+GUARD_BYTES = 4096  # per side; a multiple of 256 so the guarded tensor keeps its alignment
+GUARD_BYTE = 0x5A
+
+
+class Guarded:
+    """A device tensor placed between two guard zones of GUARD_BYTES bytes each, filled with
+    GUARD_BYTE: after a library call, check() compares every guard byte exactly, so a write that
+    runs off either end of a pool or an output (one vector past the last slot or row) fails."""
+
+    def __init__(self, t):
+        import torch
+        nbytes = t.numel() * t.element_size()
+        self.raw = torch.full((GUARD_BYTES + nbytes + GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device=t.device)
+        inner = self.raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(t.dtype).view(t.shape)
+        inner.copy_(t)
+        self.t = inner
+        self.nbytes = nbytes
+
+    def check(self, what=""):
+        import torch
+        lo = self.raw[:GUARD_BYTES]
+        hi = self.raw[GUARD_BYTES + self.nbytes:]
+        assert bool((lo == GUARD_BYTE).all()), f"guard bytes before {what} were written"
+        assert bool((hi == GUARD_BYTE).all()), f"guard bytes after {what} were written"
+        torch.cuda.synchronize()
+
+
+def guarded(t):
+    """Copy of device tensor t inside guard zones; returns the Guarded holder (use .t)."""
+    return Guarded(t)

@@ -109,3 +109,15 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["config"]["workload"] == bench.decode_config(1, bench.DECODE["layers"])["workload"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_gpus_flag_must_match_the_launched_ranks():
+    """--gpus N without N launched ranks is refused instead of silently measuring one GPU."""
+    import subprocess
+    import sys
+    env = dict(os.environ, WORLD_SIZE="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "8", "--impl", "reference"],
+                       capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode != 0
+    assert "WORLD_SIZE=1" in r.stderr and "torch.distributed.run" in r.stderr

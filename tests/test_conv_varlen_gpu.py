@@ -14,7 +14,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import f64, to_dev, to_i32
+from gpu_util import f64, guarded, to_dev, to_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -61,13 +61,18 @@ class ConvProblem:
         self.init = np.asarray(init_pattern, np.uint8)
         self.desc = bd.layer_desc(shape, act=act)
         self.use_pool = pool
-        self.pool = to_dev(self.conv0, act) if pool else None
         tdt = torch.bfloat16 if act == wl.BF16 else torch.float32
         HP, GN = shape.nheads * shape.head_dim, shape.n_groups * shape.d_state
         nan = float("nan")
-        self.x = torch.full((self.T, HP), nan, dtype=tdt, device="cuda")
-        self.B = torch.full((self.T, GN), nan, dtype=tdt, device="cuda")
-        self.C = torch.full((self.T, GN), nan, dtype=tdt, device="cuda")
+        # every written buffer sits between canary zones, checked after each call
+        self.guards = {}
+        if pool:
+            self.guards["the conv pool"] = guarded(to_dev(self.conv0, act))
+        self.guards["x"] = guarded(torch.full((self.T, HP), nan, dtype=tdt, device="cuda"))
+        self.guards["B"] = guarded(torch.full((self.T, GN), nan, dtype=tdt, device="cuda"))
+        self.guards["C"] = guarded(torch.full((self.T, GN), nan, dtype=tdt, device="cuda"))
+        self.pool = self.guards["the conv pool"].t if pool else None
+        self.x, self.B, self.C = self.guards["x"].t, self.guards["B"].t, self.guards["C"].t
 
     def run_gpu(self, err=None, cu=None):
         import torch
@@ -77,6 +82,8 @@ class ConvProblem:
                              has_initial_state=torch.from_numpy(self.init).cuda() if self.use_pool else None,
                              conv_b=to_dev(self.b, wl.F32), err_word=err)
         torch.cuda.synchronize()
+        for what, g_ in self.guards.items():
+            g_.check(what)
 
     def got(self):
         return np.concatenate([f64(self.x), f64(self.B), f64(self.C)], axis=1)

@@ -18,7 +18,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import device_normal_pool, f64, tile_rel_err, tile_rms_err, to_dev, to_i32, torch_dtype
+from gpu_util import device_normal_pool, f64, guarded, tile_rel_err, tile_rms_err, to_dev, to_i32, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -105,6 +105,8 @@ def test_nemotron_decode_batch256_one_step(state):
     import torch
     S, batch, seed = 512, 256, 11
     shape, ssm, conv = _nemotron_pools(S, seed, state)
+    g_ssm, g_conv = guarded(ssm), guarded(conv)  # canaries around both pools
+    ssm, conv = g_ssm.t, g_conv.t
     layer = Layer(shape, seed)
     desc = bd.layer_desc(shape, state=state, act=wl.BF16)
     slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
@@ -114,9 +116,12 @@ def test_nemotron_decode_batch256_one_step(state):
     o_ssm, o_conv = f64(ssm[sl]), f64(conv[sl])
     compact = np.arange(batch, dtype=np.int32)
     dev, o = _step_inputs(layer, seed, 0, batch)
-    y = torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    g_y = guarded(torch.empty(batch, 1, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16))
+    y = g_y.t
     _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y)
     torch.cuda.synchronize()
+    for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+        g_.check(what)
     y_o = _oracle_step(layer, o_ssm, o_conv, compact, o)
     tol = BF16_STEP_TOL if state == wl.BF16 else FP32_TOL
     assert tile_rel_err(f64(ssm[sl]), o_ssm, 2) < tol
@@ -136,6 +141,8 @@ def test_padding_sweep_16_steps(batch):
     import torch
     S, seed = 1536, 20 + batch
     shape, ssm, conv = _nemotron_pools(S, seed)
+    g_ssm, g_conv = guarded(ssm), guarded(conv)
+    ssm, conv = g_ssm.t, g_conv.t
     layer = Layer(shape, seed)
     desc = bd.layer_desc(shape)
     slot = wl.slot_ids(wl.rng(seed, 3), S, batch, 0.1)
@@ -149,10 +156,13 @@ def test_padding_sweep_16_steps(batch):
     for step in range(16):
         dev, o = _step_inputs(layer, seed, step, batch)
         pre_ssm, pre_conv = f64(ssm[sl_s]), f64(conv[sl_s])
-        y = torch.full((batch, 1, shape.nheads * shape.head_dim), 0x7FC1, device="cuda",
-                       dtype=torch.int16).view(torch.bfloat16)  # a NaN pattern the kernel never writes
+        g_y = guarded(torch.full((batch, 1, shape.nheads * shape.head_dim), 0x7FC1, device="cuda",
+                                 dtype=torch.int16).view(torch.bfloat16))  # a NaN pattern the kernel never writes
+        y = g_y.t
         _gpu_step(desc, layer, ssm, conv, slot_t, dev, y)
         torch.cuda.synchronize()
+        for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+            g_.check(what)
         # oracle on the sampled rows only, from the GPU's pre-step state
         n = len(sample)
         o_ssm, o_conv = pre_ssm.copy(), pre_conv.copy()
@@ -371,16 +381,21 @@ def test_speculative_decode_and_commit():
     batch, K, seed = cfg["batch"], cfg["ntok"], cfg["seed"]
     S = batch * (1 + K) + 64
     shape, ssm, conv = _nemotron_pools(S, seed, spec=K)
+    g_ssm, g_conv = guarded(ssm), guarded(conv)
+    ssm, conv = g_ssm.t, g_conv.t
     layer = Layer(shape, seed)
     desc = bd.layer_desc(shape)
     ids = wl.rng(seed, 3).choice(S, size=batch * (1 + K), replace=False).astype(np.int32)
     slot, scratch = ids[:batch], ids[batch:].reshape(batch, K)
     o_ssm, o_conv = f64(ssm), f64(conv)
     dev, o = _step_inputs(layer, seed, 0, batch, ntok=K)
-    y = torch.empty(batch, K, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16)
+    g_y = guarded(torch.empty(batch, K, shape.nheads * shape.head_dim, device="cuda", dtype=torch.bfloat16))
+    y = g_y.t
     ssm0 = ssm.clone()
     _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y, scratch_t=to_i32(scratch))
     torch.cuda.synchronize()
+    for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+        g_.check(what)
     y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
     sl = torch.from_numpy(slot).long().cuda()
     assert torch.equal(ssm[sl], ssm0[sl])  # main slots untouched
@@ -397,6 +412,8 @@ def test_speculative_decode_and_commit():
     oracle.spec_commit(e_ssm, slot, scratch, accept, conv_pool=e_conv)
     bd.mamba_spec_commit(desc, ssm, to_i32(slot), to_i32(scratch), to_i32(accept), conv_pool=conv)
     torch.cuda.synchronize()
+    g_ssm.check("the state pool after the commit")
+    g_conv.check("the conv pool after the commit")
     np.testing.assert_array_equal(f64(ssm), e_ssm)
     np.testing.assert_array_equal(f64(conv), e_conv)
 
@@ -491,7 +508,8 @@ def test_other_compiled_tiles(P, N, H, G, W, state, act, batch, ntok, spec):
     desc = bd.layer_desc(shape, state=state, act=act)
     assert bd.mamba_decode_supported(desc) == bd.MAMBA_OK
     st = wl.initial_states(wl.rng(seed, 2), shape, S, state, act)
-    ssm, conv = to_dev(st["ssm"], state), to_dev(st["conv"], act)
+    g_ssm, g_conv = guarded(to_dev(st["ssm"], state)), guarded(to_dev(st["conv"], act))
+    ssm, conv = g_ssm.t, g_conv.t
     o_conv = wl.upcast(st["conv"], act)
     ids = wl.rng(seed, 3).choice(S, size=batch * (1 + (ntok if spec else 0)), replace=False).astype(np.int32)
     slot = ids[:batch].copy()
@@ -504,10 +522,13 @@ def test_other_compiled_tiles(P, N, H, G, W, state, act, batch, ntok, spec):
         ssm_before = ssm.clone()
         o_ssm = f64(ssm)
         dev, o = _step_inputs(layer, seed, step, batch, ntok=ntok)
-        y = torch.zeros(batch, ntok, H * P, device="cuda", dtype=torch_dtype(act))
+        g_y = guarded(torch.zeros(batch, ntok, H * P, device="cuda", dtype=torch_dtype(act)))
+        y = g_y.t
         _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y,
                   scratch_t=None if scratch is None else to_i32(scratch))
         torch.cuda.synchronize()
+        for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+            g_.check(what)
         y_o = _oracle_step(layer, o_ssm, o_conv, slot, o, scratch=scratch)
         got_y = f64(y)
         rows = np.flatnonzero(slot >= 0)

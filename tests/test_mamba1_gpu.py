@@ -11,7 +11,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import f64, tile_rel_err, to_dev, to_i32
+from gpu_util import f64, guarded, tile_rel_err, to_dev, to_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,8 @@ class M1:
         for i in pad:
             self.slot[i] = -1
         self.desc = bd.mamba1_desc(Dn, N, state=state, act=act)
-        self.pool = to_dev(self.pool0, state)
+        self.g_pool = guarded(to_dev(self.pool0, state))  # canaries around the pool
+        self.pool = self.g_pool.t
         self.dp = {k: to_dev(v, wl.F32) for k, v in self.prm.items()}
         self.batch = batch
 
@@ -44,13 +45,16 @@ class M1:
         import torch
         inp = inp or wl.mamba1_inputs(self.g, self.prm, self.batch, self.N, self.act)
         tdt = torch.bfloat16 if self.act == wl.BF16 else torch.float32
-        y = torch.full((self.batch, self.Dn), float("nan"), dtype=tdt, device="cuda")
+        g_y = guarded(torch.full((self.batch, self.Dn), float("nan"), dtype=tdt, device="cuda"))
+        y = g_y.t
         before = f64(self.pool)
         bd.mamba1_state_update(self.desc, self.pool, to_i32(self.slot), to_dev(inp["x"], self.act),
                                to_dev(inp["dt"], wl.F32), self.dp["A"], to_dev(inp["B"], self.act),
                                to_dev(inp["C"], self.act), y, D=self.dp["D"], dt_bias=self.dp["dt_bias"],
                                z=to_dev(inp["z"], self.act), err_word=err)
         torch.cuda.synchronize()
+        self.g_pool.check("the state pool")
+        g_y.check("y")
         return inp, before, f64(y)
 
     def oracle_row(self, inp, before, i):

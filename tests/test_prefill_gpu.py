@@ -20,7 +20,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import f64, tile_rel_err, to_dev, to_i32
+from gpu_util import f64, guarded, tile_rel_err, to_dev, to_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -66,13 +66,15 @@ class Problem:
         self.ckpt = ids[nseq:nseq + nseq * self.max_ckpt].reshape(nseq, self.max_ckpt) if interval else None
         self.has = np.zeros(nseq, np.uint8) if has_init is None else np.asarray(has_init, np.uint8)
         self.desc = bd.layer_desc(shape, state=state, act=act)
-        self.pool = to_dev(self.pool0, state)
+        self.g_pool = guarded(to_dev(self.pool0, state))  # canaries before the first and after the last slot
+        self.pool = self.g_pool.t
         dev = "cuda"
         self.d = dict(x=to_dev(self.inp["x"], act), B=to_dev(self.inp["B"], act), C=to_dev(self.inp["C"], act),
                       dt=to_dev(self.inp["dt"], wl.F32), z=to_dev(self.inp["z"], act))
         self.dp = {k: to_dev(v, wl.F32) for k, v in self.prm.items()}
-        self.y = torch.zeros(self.T, shape.nheads, shape.head_dim, device=dev,
-                             dtype=torch.bfloat16 if act == wl.BF16 else torch.float32)
+        self.g_y = guarded(torch.zeros(self.T, shape.nheads, shape.head_dim, device=dev,
+                                       dtype=torch.bfloat16 if act == wl.BF16 else torch.float32))
+        self.y = self.g_y.t
 
     def run_gpu(self, err=None):
         import torch
@@ -84,6 +86,8 @@ class Problem:
                             ckpt_slots=to_i32(self.ckpt), ckpt_interval=self.interval, chunk=256,
                             D=self.dp["D"], dt_bias=self.dp["dt_bias"], z=self.d["z"], err_word=err)
         torch.cuda.synchronize()
+        self.g_pool.check("the state pool")
+        self.g_y.check("y")
 
     def run_oracle(self, heads=None):
         """Oracle over all heads, or over the heads of whole groups listed in `heads`."""

@@ -17,7 +17,7 @@ from recurrent_state_update_gb300 import binding as bd
 from recurrent_state_update_gb300 import build as bld
 from recurrent_state_update_gb300 import workloads as wl
 
-from gpu_util import f64, tile_rel_err, to_dev, to_i32
+from gpu_util import f64, guarded, tile_rel_err, to_dev, to_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -45,13 +45,16 @@ def test_slot_copy_is_bit_exact_and_skips(state):
     shape = SMALL
     S = 12
     st = wl.initial_states(wl.rng(80), shape, S, state, wl.BF16)
-    ssm, conv = to_dev(st["ssm"], state), to_dev(st["conv"], wl.BF16)
+    g_ssm, g_conv = guarded(to_dev(st["ssm"], state)), guarded(to_dev(st["conv"], wl.BF16))
+    ssm, conv = g_ssm.t, g_conv.t
     ssm0, conv0 = _bits(ssm), _bits(conv)
     src = np.array([3, 7, -1, 5, 9, 2], np.int32)
     dst = np.array([8, 0, 4, -1, 9, 10], np.int32)  # a -1 src, a -1 dst, src == dst
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     bd.mamba_slot_copy(bd.layer_desc(shape, state=state), ssm, to_i32(src), to_i32(dst), conv_pool=conv, err_word=err)
     torch.cuda.synchronize()
+    g_ssm.check("the state pool")
+    g_conv.check("the conv pool")
     assert int(err.item()) == 0
     exp_ssm, exp_conv = ssm0.copy(), conv0.copy()
     for s_, d_ in zip(src, dst):
@@ -77,10 +80,12 @@ def _int8_roundtrip(shape, state, S, src, ent, seed):
     desc = bd.layer_desc(shape, state=state)
     eb = bd.mamba_int8_entry_bytes(desc)
     nent = int(max(ent)) + 2
-    store = torch.zeros(nent * eb, dtype=torch.uint8, device="cuda")
+    g_store = guarded(torch.zeros(nent * eb, dtype=torch.uint8, device="cuda"))  # canaries around the store
+    store = g_store.t
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     bd.mamba_ckpt_store_int8(desc, ssm, to_i32(src), to_i32(ent), store, conv_pool=conv, err_word=err)
     torch.cuda.synchronize()
+    g_store.check("the int8 store")
     assert int(err.item()) == 0
     return st, ssm, conv, desc, eb, store, err
 
