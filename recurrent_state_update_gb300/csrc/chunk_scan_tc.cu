@@ -6,14 +6,17 @@
 // checkpoints; echobase "Mamba" notes: Y = (M (.) L) X with M_ij = C_i (prod_{k=j+1..i} Abar_k) Bbar_j):
 //   per sub-chunk of up to 128 tokens and head h, with cum_t = sum_{k<=t} Delta_k A_h:
 //     G     = C B^T                                         (tensor core, fp32 in TMEM)
-//     M     = G (.) exp(cum_i - cum_j) (.) Delta_j, j <= i   (CUDA cores, bf16 into shared memory)
+//     M     = G (.) exp(cum_i - cum_j) (.) Delta_j, j <= i   (CUDA cores, bf16 into tensor memory)
 //     Y     = M X + exp(cum_i) C h_prev^T + D x             (tensor core + epilogue)
 //     h^T   = exp(cum_end) h^T + B^T (w (.) X),  w_j = exp(cum_end - cum_j) Delta_j   (tensor core)
 //
 // Design (GB300): one CTA per (sequence, head) walks its sequence in order, so the running
 // state never leaves the SM: it lives in tensor memory in fp32 for the whole sequence (its bf16
 // copy in shared memory feeds the next C h^T).  Per sub-chunk only C, B and X are read (TMA,
-// 128-byte swizzle) and y is written: no per-chunk states travel through HBM.  The 256-token
+// 128-byte swizzle) and y is written: no per-chunk states travel through HBM.  The masked G is
+// written as bf16 over the tensor-memory columns of G the mask has consumed and M X reads it
+// from there (A operand in tensor memory), so the C tile is free as soon as C B^T and C h^T
+// complete and the next sub-chunk's C is loaded while this one is still being masked.  The 256-token
 // chunks of the checkpoint grid are processed as two 128-token halves (the MMA M of one CTA);
 // the result is the same up to rounding.  Shared memory ~98 KB and 256 TMEM columns per CTA,
 // so two CTAs share an SM and cover each other's waits; each CTA's eight warps split every
@@ -40,14 +43,14 @@ constexpr float kDiagSpan = 96.0f;  // largest base-2 exponent span of a diagona
 
 // shared-memory map (from a 1024-aligned base)
 constexpr uint32_t OFF_B = 0;          // B tile, rows j: [n 0..63 | n 64..127]
-constexpr uint32_t OFF_C = 2 * BLK;    // C tile, rows i: [n 0..63 | n 64..127]; then M, rows i: [j 0..63 | j 64..127]
+constexpr uint32_t OFF_C = 2 * BLK;    // C tile, rows i: [n 0..63 | n 64..127]
 constexpr uint32_t OFF_X = 4 * BLK;    // X tile, rows j, p 0..63; then w * X
 constexpr uint32_t OFF_H = 5 * BLK;    // h^T in bf16, rows n, p 0..63
 constexpr uint32_t OFF_SMALL = 6 * BLK;
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;  // + slack for the 1024-byte alignment
 
 struct Small {
-    uint64_t bar_tma, bar_g, bar_yd, bar_s;
+    uint64_t bar_c, bar_bx, bar_g, bar_yd, bar_s;
     uint32_t tmem;
     int pad;
     float cum2[SQ];   // cum * log2(e)
@@ -69,15 +72,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void issue_loads(unsigned char *sm, Small *sv, const CUtensorMap *mX, const CUtensorMap *mB,
-                                            const CUtensorMap *mC, int h, int g, int t0) {
-    mbar_arrive_expect_tx(&sv->bar_tma, 5 * BLK);
-    tma_load_2d(sm + OFF_B, mB, g * TN, t0, &sv->bar_tma);
-    tma_load_2d(sm + OFF_B + BLK, mB, g * TN + 64, t0, &sv->bar_tma);
-    tma_load_2d(sm + OFF_C, mC, g * TN, t0, &sv->bar_tma);
-    tma_load_2d(sm + OFF_C + BLK, mC, g * TN + 64, t0, &sv->bar_tma);
-    tma_load_2d(sm + OFF_X, mX, h * TP, t0, &sv->bar_tma);
+// The C tile of the sub-chunk starting at token t0 (completes on bar_c) ...
+__device__ __forceinline__ void issue_c(unsigned char *sm, Small *sv, const CUtensorMap *mC, int g, int t0) {
+    mbar_arrive_expect_tx(&sv->bar_c, 2 * BLK);
+    tma_load_2d(sm + OFF_C, mC, g * TN, t0, &sv->bar_c);
+    tma_load_2d(sm + OFF_C + BLK, mC, g * TN + 64, t0, &sv->bar_c);
 }
+
+// ... and its B and X tiles (complete on bar_bx).
+__device__ __forceinline__ void issue_bx(unsigned char *sm, Small *sv, const CUtensorMap *mX, const CUtensorMap *mB,
+                                         int h, int g, int t0) {
+    mbar_arrive_expect_tx(&sv->bar_bx, 3 * BLK);
+    tma_load_2d(sm + OFF_B, mB, g * TN, t0, &sv->bar_bx);
+    tma_load_2d(sm + OFF_B + BLK, mB, g * TN + 64, t0, &sv->bar_bx);
+    tma_load_2d(sm + OFF_X, mX, h * TP, t0, &sv->bar_bx);
+}
+
+// Tensor-memory column (relative to G) where the packed bf16 masked G of 32-column block jb goes:
+// the two blocks a warp handles, hf and hf + 2, both land in block hf + 2's columns, which that
+// same warp has already read.
+__device__ __forceinline__ uint32_t m_col(int jb) { return 64u + 32u * (uint32_t)(jb & 1) + 16u * (uint32_t)(jb >> 1); }
 
 // Writes the 64 p-values of h^T row n (fp32) as bf16 into the swizzled MN-major h tile.
 __device__ __forceinline__ void store_hT_row(unsigned char *sm, int n, const float *v, int c0) {
@@ -160,7 +174,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
     const int64_t head_off = (int64_t)h * TP * TN;
 
     if (tid == 0) {
-        mbar_init(&sv->bar_tma, 1);
+        mbar_init(&sv->bar_c, 1);
+        mbar_init(&sv->bar_bx, 1);
         mbar_init(&sv->bar_g, 1);
         mbar_init(&sv->bar_yd, 1);
         mbar_init(&sv->bar_s, 1);
@@ -192,12 +207,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         fence_async_smem();
     }
     const int nsub = (len + SQ - 1) / SQ;
-    // pending operations of thread 0 (bit 0: TMA, 1: G/Y_off, 2: Y_diag, 3: state) and their parities
-    uint32_t pending = 0, pend_par[4] = {0, 0, 0, 0};
+    // pending operations of thread 0 (bit 0: C tile, 1: G/Y_off, 2: Y_diag, 3: state, 4: B and X
+    // tiles) and their parities
+    uint32_t pending = 0, pend_par[5] = {0, 0, 0, 0, 0};
     if (tid == 0) {
-        issue_loads(sm, sv, &mX, &mB, &mC, h, g, t_begin);
-        pending |= 1u;
-        pend_par[0] = 0;
+        issue_c(sm, sv, &mC, g, t_begin);
+        issue_bx(sm, sv, &mX, &mB, h, g, t_begin);
+        pending |= 1u | 16u;
     }
     tc_fence_before();
     __syncthreads();
@@ -243,10 +259,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
             sv->delta[tid] = dlt;
         }
         // G = C B^T and Y_off = C h_prev^T (every thread waits for the tiles itself: it reads X)
-        int bad = mbar_wait(&sv->bar_tma, ph, kPolls) ? 0 : 1;
+        int bad = (mbar_wait(&sv->bar_c, ph, kPolls) && mbar_wait(&sv->bar_bx, ph, kPolls)) ? 0 : 1;
         if (tid == 0) {
             if (!bad) {
-                pending &= ~1u;
+                pending &= ~(1u | 16u);
                 tc_fence_after();
                 const uint32_t c = smem_u32(sm + OFF_C), b = smem_u32(sm + OFF_B), hh = smem_u32(sm + OFF_H);
 #pragma unroll
@@ -290,15 +306,21 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
             xrow[qq] = *reinterpret_cast<const uint4 *>(sm + OFF_X + swz128_chunk(row, hf * 4 + qq));
         __syncthreads();  // ecol visible
 
-        // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, written over the consumed C tile.
-        // Row i = this thread's lane; this warp forms column blocks jb = hf and hf + 2.
+        // M = G (.) exp(cum_i - cum_j) (.) Delta_j for j <= i, as packed bf16 into tensor memory
+        // over G's columns.  Row i = this thread's lane; this warp forms column blocks jb = hf + 2
+        // and then hf, and writes both into block hf + 2's columns (m_col), read just before.
         if (!mbar_wait(&sv->bar_g, ph, kPolls)) bad = 1;
         else if (tid == 0) pending &= ~2u;
         tc_fence_after();
+        if (tid == 0 && !bad && k + 1 < nsub) {  // C B^T and C h^T are done with the C tile
+            issue_c(sm, sv, &mC, g, t0 + SQ);
+            pending |= 1u;
+            pend_par[0] = ph ^ 1u;
+        }
         {
             const float ci = sv->cum2[row];
 #pragma unroll
-            for (int bb = 0; bb < 2; ++bb) {
+            for (int bb = 1; bb >= 0; --bb) {
                 const int jb = hf + 2 * bb;
                 uint32_t pk[16];
                 if (jb <= q) {  // warp-uniform: block jb can hold columns j <= i for these rows
@@ -334,23 +356,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
 #pragma unroll
                     for (int qq = 0; qq < 16; ++qq) pk[qq] = 0u;
                 }
-                unsigned char *blk = sm + OFF_C + (uint32_t)(jb >> 1) * BLK;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(blk + swz128_chunk(row, (jb & 1) * 4 + q4)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                tmem_st16(t_g + lane_base + m_col(jb), pk);
             }
         }
-        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // Y_diag = M X (into the G columns, which are consumed)
+        // Y_diag = M X (A = M from tensor memory; into G's first 64 columns, which are consumed)
         if (tid == 0 && !bad) {
-            const uint32_t m = smem_u32(sm + OFF_C), x = smem_u32(sm + OFF_X);
+            const uint32_t x = smem_u32(sm + OFF_X);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(t_yd, desc_kmajor(m, BLK, kk), desc_mnmajor(x, BLK, kk), ID_YD, kk > 0);
+                mma_bf16_ts(t_yd, t_g + m_col(kk >> 1) + 8u * (uint32_t)(kk & 1), desc_mnmajor(x, BLK, kk), ID_YD,
+                            kk > 0);
             mma_commit(&sv->bar_yd);
             pending |= 4u;
             pend_par[2] = ph;
@@ -441,9 +459,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         if (tid == 0 && !bad) {
             pending &= ~8u;
             if (k + 1 < nsub) {
-                issue_loads(sm, sv, &mX, &mB, &mC, h, g, t0 + SQ);
-                pending |= 1u;
-                pend_par[0] = ph ^ 1u;
+                issue_bx(sm, sv, &mX, &mB, h, g, t0 + SQ);
+                pending |= 16u;
+                pend_par[4] = ph ^ 1u;
             }
         }
         // h^T -> bf16 copy for the next C h^T; checkpoints and the final state -> pool
@@ -482,7 +500,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, 
         // flight finish (bounded) before the tensor memory is released
         if (tid == 0) {
             flag_error(p.err, MAMBA_ERR_TIMEOUT);
-            if (pending & 1u) mbar_wait(&sv->bar_tma, pend_par[0], kPolls);
+            if (pending & 1u) mbar_wait(&sv->bar_c, pend_par[0], kPolls);
+            if (pending & 16u) mbar_wait(&sv->bar_bx, pend_par[4], kPolls);
             if (pending & 2u) mbar_wait(&sv->bar_g, pend_par[1], kPolls);
             if (pending & 4u) mbar_wait(&sv->bar_yd, pend_par[2], kPolls);
             if (pending & 8u) mbar_wait(&sv->bar_s, pend_par[3], kPolls);
