@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+
 #include "mamba_state.h"
 
 // NVTX ranges: every exported call that launches work opens a range named after the call for
@@ -126,6 +128,43 @@ inline int check_desc(const mamba_layer_desc *d) {
         !dtype_ok(d->dt_dtype))
         return MAMBA_EINVAL;
     return MAMBA_OK;
+}
+
+// Programmatic dependent launch.  The decode-path kernels are launched with the programmatic
+// stream-serialization attribute, so the hardware may start their CTAs while the previous kernel
+// in the stream is still finishing; each of them first executes pdl_wait(), which blocks until
+// every prerequisite grid has completed and its memory is visible, before it touches global
+// memory, so the result is the same as a plain launch: only the launch latency and the
+// prologue overlap the previous kernel's tail.  pdl_wait() is a no-op in a kernel launched
+// without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled (it still waits for this one to complete).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether launches request programmatic dependent launch: yes unless the environment variable
+// MAMBA_PDL is "0" when the library first launches (read once per process).
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("MAMBA_PDL");
+        return !(v && v[0] == '0' && v[1] == 0);
+    }();
+    return on;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 inline int launch_status() {

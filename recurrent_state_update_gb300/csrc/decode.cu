@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(512) k_decode(const DecodeArgs a) {
     const int ntok = NT > 0 ? NT : a.ntok;
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t s = a.slot[i];
     if (s == -1) return;  // padding row
     bool bad = s < -1 || s >= a.num_slots;
@@ -789,6 +791,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_stream(const Strea
     const size_t DTES = a.dt_bf16 ? 2 : 4;
     const StreamSmem L(NS, TILE_BYTES, LC, HG, P, Wk, Wc, ES, DTES);
 
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(128) unsigned char st_smem[];
     unsigned char *stages = st_smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(st_smem + L.bars);
@@ -1092,6 +1096,8 @@ constexpr int kConvThreads = 128;
 
 template <typename ActT, int W>
 __global__ void __launch_bounds__(kConvThreads) k_conv_step(const ConvArgs a, int batch) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int V = Vec16<ActT>::n;
     const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
     if (c0 >= a.Cd) return;
@@ -1177,13 +1183,12 @@ bool launch_conv_step(const ConvArgs &a, int batch, size_t ab, cudaStream_t st) 
         return false;
     const dim3 grid((a.Cd / V + kConvThreads - 1) / kConvThreads, (batch + kConvRows - 1) / kConvRows);
     switch (a.W) {
-        case 2: k_conv_step<ActT, 2><<<grid, kConvThreads, 0, st>>>(a, batch); break;
-        case 3: k_conv_step<ActT, 3><<<grid, kConvThreads, 0, st>>>(a, batch); break;
-        case 4: k_conv_step<ActT, 4><<<grid, kConvThreads, 0, st>>>(a, batch); break;
-        case 5: k_conv_step<ActT, 5><<<grid, kConvThreads, 0, st>>>(a, batch); break;
+        case 2: return launch_pdl(k_conv_step<ActT, 2>, grid, dim3(kConvThreads), 0, st, a, batch) == cudaSuccess;
+        case 3: return launch_pdl(k_conv_step<ActT, 3>, grid, dim3(kConvThreads), 0, st, a, batch) == cudaSuccess;
+        case 4: return launch_pdl(k_conv_step<ActT, 4>, grid, dim3(kConvThreads), 0, st, a, batch) == cudaSuccess;
+        case 5: return launch_pdl(k_conv_step<ActT, 5>, grid, dim3(kConvThreads), 0, st, a, batch) == cudaSuccess;
         default: return false;
     }
-    return true;
 }
 
 template <typename ActT>
@@ -1391,7 +1396,7 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int grid = W < sm_count ? W : sm_count;
     auto kern = k_decode_stream<StateT, ActT, P, N>;
     if (!smem_limit(reinterpret_cast<const void *>(kern), smem)) return MAMBA_ECUDA;
-    kern<<<grid, kStreamThreads, smem, stream>>>(sa);
+    if (launch_pdl(kern, dim3(grid), dim3(kStreamThreads), smem, stream, sa) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -1451,14 +1456,17 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     cfg.blockDim = dim3(nhs * TL::TH);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ksplit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (ksplit > 1 && !cluster_fits(reinterpret_cast<const void *>(kern), cfg)) continue;  // one CTA per (row, group)
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
     }

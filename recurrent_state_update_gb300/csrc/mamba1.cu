@@ -107,6 +107,8 @@ __device__ __forceinline__ void load_bc(const ActT *p, float (&f)[N]) {
 // flight while the current row is computed.
 template <typename StateT, typename ActT, int N>
 __global__ void __launch_bounds__(kM1Threads, N <= 16 ? 3 : 1) k_mamba1_update(const M1Args a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int d = blockIdx.x * kM1Threads + threadIdx.x;
     if (d >= a.Dn) return;
     float Ar[N];  // this channel's row of A, times log2(e)
@@ -189,6 +191,8 @@ __device__ __forceinline__ float act_at(const unsigned char *p, int t) {
 
 template <typename StateT, typename ActT, int N>
 __global__ void __launch_bounds__(kM1StreamThreads, 2) k_mamba1_stream(const M1StreamArgs sa) {
+    pdl_wait();
+    pdl_launch_dependents();
     const M1Args &a = sa.a;
     const int NS = sa.ns, kpb = sa.kpb;
     const int cb = blockIdx.x % sa.ncb, rb = blockIdx.x / sa.ncb;
@@ -357,8 +361,7 @@ bool launch_m1_stream(const M1Args &a, int batch, cudaStream_t st) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
     M1StreamArgs sa;
     sa.a = a; sa.ns = ns; sa.kpb = kpb; sa.ncb = ncb;
-    kern<<<ncb * kpb, kM1StreamThreads, smem, st>>>(sa);
-    return true;
+    return launch_pdl(kern, dim3(ncb * kpb), dim3(kM1StreamThreads), smem, st, sa) == cudaSuccess;
     }
 }
 
@@ -371,7 +374,7 @@ void launch_m1n(const M1Args &a, int batch, cudaStream_t st) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_mamba1_update<StateT, ActT, N>, kM1Threads, 0);
     const int slots = std::max(1, sm_count_m1()) * std::max(1, occ);
     const int gy = std::min(batch, std::max(1, slots / cb));
-    k_mamba1_update<StateT, ActT, N><<<dim3(cb, gy), kM1Threads, 0, st>>>(a);
+    launch_pdl(k_mamba1_update<StateT, ActT, N>, dim3(cb, gy), dim3(kM1Threads), 0, st, a);
 }
 
 template <typename StateT, typename ActT>
