@@ -94,6 +94,8 @@ struct ScanArgs {
 // ---------------------------------------------------------------------------------------
 
 __global__ void k_chunk_meta(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     bool ok = a.cu[0] == 0 && a.cu[a.nseq] == a.T;
@@ -131,6 +133,8 @@ __global__ void k_chunk_meta(const ScanArgs a) {
 // ---------------------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(1024) k_chunk_prep(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int c = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
     if (c >= *tb.count) return;
@@ -161,6 +165,8 @@ __global__ void __launch_bounds__(1024) k_chunk_prep(const ScanArgs a) {
 
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_chunk_cb(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int c = blockIdx.x, g = blockIdx.y;
     const int ti = blockIdx.z / 4, tj = blockIdx.z % 4;  // 64-row tiles of a chunk of up to 256
@@ -208,6 +214,8 @@ __global__ void __launch_bounds__(256) k_chunk_cb(const ScanArgs a) {
 
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_chunk_state(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= *tb.count) return;
@@ -262,6 +270,8 @@ __global__ void __launch_bounds__(256) k_chunk_state(const ScanArgs a) {
 
 template <typename StateT>
 __global__ void __launch_bounds__(256) k_state_pass(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int s = blockIdx.x, h = blockIdx.y;
     const int64_t PN = (int64_t)a.P * a.N;
@@ -305,6 +315,8 @@ __global__ void __launch_bounds__(256) k_state_pass(const ScanArgs a) {
 
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     ChunkTable tb(a.meta, a.nchunks_max, a.nseq);
     const int c = blockIdx.x, h = blockIdx.y, ti = blockIdx.z;
     if (c >= *tb.count) return;
@@ -399,14 +411,16 @@ __global__ void __launch_bounds__(256) k_chunk_out(const ScanArgs a) {
 
 template <typename ActT, typename StateT>
 static int launch_scan(const ScanArgs &a, cudaStream_t st) {
-    k_chunk_meta<<<1, 32, 0, st>>>(a);
-    k_chunk_prep<<<dim3(a.nchunks_max, a.H), a.Q, sizeof(double) * a.Q, st>>>(a);
-    k_chunk_cb<ActT><<<dim3(a.nchunks_max, a.G, 16), 256, 0, st>>>(a);
     const size_t smem_state = sizeof(float) * 32 * (size_t)(a.P + a.N);
-    k_chunk_state<ActT><<<dim3(a.nchunks_max, a.H), 256, smem_state, st>>>(a);
     const int64_t PN = (int64_t)a.P * a.N;
-    k_state_pass<StateT><<<dim3(a.nseq, a.H, (unsigned)((PN + 255) / 256)), 256, 0, st>>>(a);
-    k_chunk_out<ActT><<<dim3(a.nchunks_max, a.H, (a.Q + 63) / 64), 256, 0, st>>>(a);
+    if (launch_pdl(k_chunk_meta, dim3(1), dim3(32), 0, st, a) != cudaSuccess ||
+        launch_pdl(k_chunk_prep, dim3(a.nchunks_max, a.H), dim3(a.Q), sizeof(double) * a.Q, st, a) != cudaSuccess ||
+        launch_pdl(k_chunk_cb<ActT>, dim3(a.nchunks_max, a.G, 16), dim3(256), 0, st, a) != cudaSuccess ||
+        launch_pdl(k_chunk_state<ActT>, dim3(a.nchunks_max, a.H), dim3(256), smem_state, st, a) != cudaSuccess ||
+        launch_pdl(k_state_pass<StateT>, dim3(a.nseq, a.H, (unsigned)((PN + 255) / 256)), dim3(256), 0, st, a) !=
+            cudaSuccess ||
+        launch_pdl(k_chunk_out<ActT>, dim3(a.nchunks_max, a.H, (a.Q + 63) / 64), dim3(256), 0, st, a) != cudaSuccess)
+        return MAMBA_ECUDA;
     return launch_status();
 }
 

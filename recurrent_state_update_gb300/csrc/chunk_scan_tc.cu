@@ -117,6 +117,8 @@ __device__ __forceinline__ void write_state(StateT *dst, int n, const float *v, 
 // Validates cu_seqlens and slot ids, and orders the sequences longest first (so the longest
 // serial chains start first).  meta = [valid, pad x3, order[nseq]].
 __global__ void __launch_bounds__(256) k_tc_meta(const ScanTcParams p) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     __shared__ int ok;
     const int tid = threadIdx.x;
     if (tid == 0) ok = p.cu[0] == 0 && p.cu[p.nseq] == p.T;
@@ -154,6 +156,8 @@ template <typename StateT>
 __global__ void __launch_bounds__(kTcThreads, 2) k_ssd_tc(const ScanTcParams p, const __grid_constant__ CUtensorMap mX,
                                                           const __grid_constant__ CUtensorMap mB,
                                                           const __grid_constant__ CUtensorMap mC) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_smem) + 1023) &
                                                           ~static_cast<uintptr_t>(1023));
@@ -558,7 +562,7 @@ bool scan_tc_eligible(const mamba_layer_desc *d, int chunk) {
 size_t scan_tc_workspace_bytes(int nseq) { return ((size_t)(4 + nseq) * sizeof(int32_t) + 255) / 256 * 256; }
 
 int scan_tc_launch(const ScanTcParams &p, int state_bf16, cudaStream_t stream) {
-    k_tc_meta<<<1, 256, 0, stream>>>(p);
+    if (launch_pdl(k_tc_meta, dim3(1), dim3(256), 0, stream, p) != cudaSuccess) return MAMBA_ECUDA;
     if (p.T == 0) return launch_status();  // only empty sequences: nothing to compute or write
     CUtensorMap mX, mB, mC;
     if (!make_map(&mX, p.x, (uint64_t)p.H * TP, (uint64_t)p.T) ||
@@ -568,7 +572,8 @@ int scan_tc_launch(const ScanTcParams &p, int state_bf16, cudaStream_t stream) {
     auto kern = state_bf16 ? k_ssd_tc<bf16> : k_ssd_tc<float>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
         return MAMBA_ECUDA;
-    kern<<<p.nseq * p.H, kTcThreads, SMEM_BYTES, stream>>>(p, mX, mB, mC);
+    if (launch_pdl(kern, dim3(p.nseq * p.H), dim3(kTcThreads), SMEM_BYTES, stream, p, mX, mB, mC) != cudaSuccess)
+        return MAMBA_ECUDA;
     return launch_status();
 }
 

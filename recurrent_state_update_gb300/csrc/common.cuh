@@ -139,7 +139,7 @@ inline int check_desc(const mamba_layer_desc *d) {
 // without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Lets the next kernel in the stream be scheduled (it still waits for this one to complete).
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // Whether launches request programmatic dependent launch: yes unless the environment variable
 // MAMBA_PDL is "0" when the library first launches (read once per process).

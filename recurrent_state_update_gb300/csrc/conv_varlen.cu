@@ -114,6 +114,8 @@ struct BulkGeom {
 // (one row per lane, split at the x | B | C boundaries) while the next tiles are convolved.
 template <typename ActT, int W>
 __global__ void __launch_bounds__(BulkGeom<W>::THREADS, BulkGeom<W>::MINB) k_conv_varlen(const VarlenArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     using Geo = BulkGeom<W>;
     constexpr int kTokPerThread = Geo::TOK, kBulkTokens = Geo::TOKENS, S = Geo::S, SO = Geo::SO;
     constexpr int V = Vec16<ActT>::n;
@@ -306,6 +308,8 @@ __global__ void __launch_bounds__(BulkGeom<W>::THREADS, BulkGeom<W>::MINB) k_con
 // Column i reads column i + L of the old window (only when L < Wc), which is not yet written.
 template <typename ActT>
 __global__ void __launch_bounds__(kVarThreads) k_conv_varlen_state(const VarlenArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     if (!seqlens_ok(a)) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(a.err, MAMBA_ERR_SEQLENS);
         return;
@@ -351,7 +355,7 @@ int launch_varlen(const VarlenArgs &a, cudaStream_t st) {
     // a whole number of CTAs per channel block, no more than there are token blocks
     const int ntb = (a.T + Geo::TOKENS - 1) / Geo::TOKENS;
     const int per_cb = max(1, min(sms * occ / a.ncb, ntb));
-    kern<<<per_cb * a.ncb, Geo::THREADS, Geo::SMEM, st>>>(a);
+    if (launch_pdl(kern, dim3(per_cb * a.ncb), dim3(Geo::THREADS), Geo::SMEM, st, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -412,9 +416,10 @@ extern "C" int mamba_conv_varlen(const mamba_layer_desc *d, void *conv_pool, int
     }
     if (conv_pool) {
         const dim3 grid((Cd + kVarThreads - 1) / kVarThreads, nseq);
-        if (d->act_dtype == MAMBA_BF16) k_conv_varlen_state<bf16><<<grid, kVarThreads, 0, st>>>(a);
-        else k_conv_varlen_state<float><<<grid, kVarThreads, 0, st>>>(a);
-        rc = launch_status();
+        const cudaError_t e = d->act_dtype == MAMBA_BF16
+                                  ? launch_pdl(k_conv_varlen_state<bf16>, grid, dim3(kVarThreads), 0, st, a)
+                                  : launch_pdl(k_conv_varlen_state<float>, grid, dim3(kVarThreads), 0, st, a);
+        rc = e != cudaSuccess ? MAMBA_ECUDA : launch_status();
     }
     return rc;
 }

@@ -1193,6 +1193,8 @@ bool launch_conv_step(const ConvArgs &a, int batch, size_t ab, cudaStream_t st) 
 
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_conv_update(const ConvArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     const int cb = blockIdx.x, i = blockIdx.y, ntok = a.ntok;
     const int32_t s = a.slot[i];
     if (s == -1) return;  // padding row
@@ -1241,6 +1243,8 @@ struct CommitArgs {
 // row is left entirely untouched.
 template <typename ActT>
 __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     const int unit = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
     const int32_t s = a.slot[i];
     if (s == -1) return;  // padding row
@@ -1572,7 +1576,7 @@ extern "C" int mamba_conv_update(const mamba_layer_desc *d, void *conv_pool, int
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MAMBA_ECUDA;
-    kern<<<grid, block, smem, st>>>(a);
+    if (launch_pdl(kern, grid, block, smem, st, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -1606,7 +1610,7 @@ extern "C" int mamba1_conv_update(const mamba1_layer_desc *d, void *conv_pool, i
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MAMBA_ECUDA;
-    kern<<<grid, block, smem, st>>>(a);
+    if (launch_pdl(kern, grid, block, smem, st, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -1641,6 +1645,6 @@ extern "C" int mamba_spec_commit(const mamba_layer_desc *d, void *ssm_pool, int6
     const dim3 grid(H + conv_units, batch), block(256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto kern = d->conv_dtype == MAMBA_BF16 ? k_spec_commit<bf16> : k_spec_commit<float>;
-    kern<<<grid, block, smem, st>>>(a);
+    if (launch_pdl(kern, grid, block, smem, st, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }

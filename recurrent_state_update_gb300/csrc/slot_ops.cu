@@ -63,6 +63,8 @@ struct CopyArgs {
 // Block (b, i) copies bytes [b * kCopyBytes, ...) of slot src[i]'s SSM bytes followed by its conv
 // bytes into slot dst[i].
 __global__ void __launch_bounds__(kCopyThreads) k_slot_copy(const CopyArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     const int i = blockIdx.y;
     const int32_t s = a.src[i], d = a.dst[i];
     if (s < -1 || s >= a.num_slots || d < -1 || d >= a.num_slots) {
@@ -160,6 +162,8 @@ __host__ __device__ inline int store_shares(int octs) {
 // of a share's rows and combines the shares with warp shuffles, pass 2 writes 8 codes per row.
 template <typename StateT>
 __global__ void __launch_bounds__(1024) k_ckpt_store_int8(const QArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     extern __shared__ __align__(128) unsigned char q_smem[];
     __shared__ uint64_t bar;
     int32_t sl, en;
@@ -240,6 +244,8 @@ __global__ void __launch_bounds__(1024) k_ckpt_store_int8(const QArgs a) {
 // Load: the inverse, state = q * s (fp32 product, then the pool dtype), into slot slots[i].
 template <typename StateT>
 __global__ void __launch_bounds__(kQThreads) k_ckpt_load_int8(const QArgs a) {
+    pdl_wait();  // see pdl_wait: no global access before the previous grid is complete
+    pdl_launch_dependents();
     int32_t sl, en;
     if (!pair_ok(a, blockIdx.y, sl, en)) return;
     const unsigned char *entry = a.store + en * (int64_t)a.lay.total;
@@ -353,7 +359,8 @@ extern "C" int mamba_slot_copy(const mamba_layer_desc *d, void *ssm_pool, int64_
     a.err = err_word;
     const int64_t total = a.ssm_bytes + (conv_pool ? a.conv_bytes : 0);
     const dim3 grid((unsigned)((total + kCopyBytes - 1) / kCopyBytes), n);
-    k_slot_copy<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    if (launch_pdl(k_slot_copy, grid, dim3(kCopyThreads), 0, static_cast<cudaStream_t>(stream), a) != cudaSuccess)
+        return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -383,7 +390,7 @@ extern "C" int mamba_ckpt_store_int8(const mamba_layer_desc *d, const void *ssm_
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MAMBA_ECUDA;
-    kern<<<grid, threads, smem, st>>>(a);
+    if (launch_pdl(kern, grid, dim3(threads), smem, st, a) != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
 
@@ -399,7 +406,8 @@ extern "C" int mamba_ckpt_load_int8(const mamba_layer_desc *d, void *ssm_pool, i
     const int conv_blocks = conv_pool ? (int)((a.conv_bytes + 64 * kQThreads - 1) / (64 * kQThreads)) : 0;
     const dim3 grid(a.H + conv_blocks, n);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (d->state_dtype == MAMBA_BF16) k_ckpt_load_int8<bf16><<<grid, kQThreads, 0, st>>>(a);
-    else k_ckpt_load_int8<float><<<grid, kQThreads, 0, st>>>(a);
+    const cudaError_t e = d->state_dtype == MAMBA_BF16 ? launch_pdl(k_ckpt_load_int8<bf16>, grid, dim3(kQThreads), 0, st, a)
+                                                       : launch_pdl(k_ckpt_load_int8<float>, grid, dim3(kQThreads), 0, st, a);
+    if (e != cudaSuccess) return MAMBA_ECUDA;
     return launch_status();
 }
