@@ -165,10 +165,12 @@ def test_prefill_fp32_state_bf16_activations(steps):
 
 
 @pytest.mark.parametrize("steps", [wl.WIDE_STEPS, wl.LARGE_STEPS])
-def test_prefill_tc_wide_steps(steps):
+@pytest.mark.parametrize("H,G", [(128, 8), (24, 8)])
+def test_prefill_tc_wide_steps(steps, H, G):
     """Tensor-core path with steps up to 5 (Delta*|A| up to ~80 per token) mixed with tiny ones:
     empty, length-1, partial and multi-chunk sequences, initial states, checkpoints, z gate."""
-    pr = Problem(wl.NEMOTRON_H_8B, [1, 0, 129, 300, 1024, 700, 2000], seed=31, act=wl.BF16, state=wl.BF16,
+    shape = wl.LayerShape(nheads=H, head_dim=64, d_state=128, n_groups=G)
+    pr = Problem(shape, [1, 0, 129, 300, 1024, 700, 2000], seed=31, act=wl.BF16, state=wl.BF16,
                  has_init=[1, 1, 0, 1, 1, 0, 1], interval=256, with_z=True, steps=steps)
     pr.run_gpu()
     pr.check(2e-2)
@@ -248,11 +250,11 @@ def test_prefill_bad_seqlens_flagged_nothing_written():
     assert not f64(pr.y).any()
 
 
-@pytest.mark.parametrize("H,G", [(80, 1), (24, 3)])
+@pytest.mark.parametrize("H,G", [(80, 1), (24, 3), (24, 8)])
 def test_prefill_tc_other_head_and_group_counts(H, G):
     """Tensor-core path at head_dim 64, d_state 128 with other head and group counts (one group
-    shared by 80 heads, three groups of 8): ragged and empty sequences, initial states,
-    checkpoints, z gate."""
+    shared by 80 heads, three groups of 8, eight groups of 3): ragged and empty sequences, initial
+    states, checkpoints, z gate."""
     shape = wl.LayerShape(nheads=H, head_dim=64, d_state=128, n_groups=G)
     pr = Problem(shape, [300, 0, 1025, 128], seed=10 + H, act=wl.BF16, state=wl.BF16, has_init=[1, 1, 0, 1],
                  interval=512, with_z=True)
