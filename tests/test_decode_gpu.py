@@ -254,6 +254,62 @@ def test_decode_wide_steps(state, batch, ntok):
         np.testing.assert_array_equal(f64(conv[torch.from_numpy(slot).long().cuda()]), o_conv[slot])
 
 
+def _tail_batch(kind, sms, G):
+    """A batch whose last round of (row, group) items over `sms` persistent CTAs is: 'short' (a
+    few items), 'half' (the longest round that is still at most half of the CTAs, after two full
+    rounds) or 'over' (the shortest round longer than half)."""
+    cands = [(b, (b * G) // sms, (b * G) % sms) for b in range(sms // G + 1, 4 * sms // G + 1)]
+    if kind == "short":
+        return next(b for b, f, r in cands if r > 0)
+    if kind == "half":
+        return max((r, b) for b, f, r in cands if f == 2 and 0 < r <= sms // 2)[1]
+    return min((r, b) for b, f, r in cands if f == 1 and r > sms // 2)[1]
+
+
+@pytest.mark.parametrize("kind", ["short", "half", "over"])
+def test_stream_tail_round_every_row(kind):
+    """The persistent stream's last, partial round of items: batches whose last round is short,
+    at most half, or over half of the CTAs, the last row padded (-1) so that round also skips
+    items; two steps, every row's y and state, the conv windows exactly, every other slot and the
+    guard zones untouched."""
+    import torch
+    shape = wl.NEMOTRON_H_8B
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    batch = _tail_batch(kind, sms, shape.n_groups)
+    S, seed = 2 * batch + 8, 130 + batch
+    shape, ssm, conv = _nemotron_pools(S, seed)
+    g_ssm, g_conv = guarded(ssm), guarded(conv)
+    ssm, conv = g_ssm.t, g_conv.t
+    layer = Layer(shape, seed)
+    desc = bd.layer_desc(shape)
+    slot = wl.slot_ids(wl.rng(seed, 3), S, batch)
+    slot[-1] = -1
+    live = np.flatnonzero(slot >= 0)
+    sl = torch.from_numpy(slot[live]).long().cuda()
+    mask = torch.ones(S, dtype=torch.bool, device="cuda")
+    mask[sl] = False
+    ssm0, conv0 = ssm.clone(), conv.clone()
+    for step in range(2):
+        o_ssm, o_conv = f64(ssm), f64(conv)
+        dev, o = _step_inputs(layer, seed, step, batch)
+        g_y = guarded(torch.full((batch, 1, shape.nheads * shape.head_dim), 0x7FC1, device="cuda",
+                                 dtype=torch.int16).view(torch.bfloat16))
+        y = g_y.t
+        _gpu_step(desc, layer, ssm, conv, to_i32(slot), dev, y)
+        torch.cuda.synchronize()
+        for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+            g_.check(what)
+        y_o = _oracle_step(layer, o_ssm, o_conv, slot, o)
+        yl = torch.from_numpy(live).long().cuda()
+        assert tile_rel_err(f64(y[yl]).reshape(len(live), shape.nheads, -1),
+                            y_o[live].reshape(len(live), shape.nheads, -1), 1) < 2e-2
+        assert bool((y[-1].view(torch.int16) == 0x7FC1).all())
+        assert tile_rel_err(f64(ssm[sl]), o_ssm[slot[live]], 2) < BF16_STEP_TOL
+        np.testing.assert_array_equal(f64(conv[sl]), o_conv[slot[live]])
+        assert torch.equal(ssm[mask], ssm0[mask])
+        assert torch.equal(conv[mask], conv0[mask])
+
+
 @pytest.mark.parametrize("batch", [4, 64])
 def test_slot_ids_below_minus_one_are_flagged(batch):
     """A slot id below -1 is outside the pool, not padding: the decode step, the standalone conv
