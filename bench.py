@@ -161,6 +161,16 @@ class ClockSampler:
 # GPU arm
 # ------------------------------------------------------------------------------------------
 
+def e2e_groups(layers: int):
+    """Group sizes of the end-to-end pipeline: one layer first and last (its upload, or its
+    download, is the part not hidden behind compute), doubling up to eight layers between."""
+    up = [1, 2, 4]
+    if layers < 2 * sum(up) + 8:
+        return [1] * layers
+    mid = layers - 2 * sum(up)
+    return up + [8] * (mid // 8) + ([mid % 8] if mid % 8 else []) + up[::-1]
+
+
 class DecodeWorkload:
     """48 layers of pools, parameters and one step's inputs, resident on the device."""
 
@@ -180,30 +190,47 @@ class DecodeWorkload:
         for l in range(layers):
             self.ssm[l].copy_(torch.randn(pool, H, P, N, generator=gen, device=dev).mul_(0.1))
             self.conv[l].copy_(torch.randn(pool, CD, W1, generator=gen, device=dev).mul_(0.1))
+        # Every layer's step inputs (xbc, dt, z, slot ids) packed back to back in one pinned host
+        # buffer and its device copy, so that the inputs of a run of layers move in one copy.
         self.prm, self.slot, self.inp, self.host_inp = [], [], [], []
+        host_np = []
         for l in range(layers):
             g = wl.rng(seed, l)
             prm = wl.layer_params(g, SHAPE)
             self.prm.append({k: torch.from_numpy(v).to(dev) for k, v in prm.items()})
             ids = wl.slot_ids(g, pool, batch)
-            self.slot.append(torch.from_numpy(ids).to(dev))
             inp = wl.decode_inputs(g, SHAPE, prm, batch, 1, wl.BF16)
-            host = {
-                "xbc": torch.from_numpy(inp["xbc"].view(np.int16)).view(bf).pin_memory(),
-                "dt": torch.from_numpy(inp["dt"]).pin_memory(),
-                "z": torch.from_numpy(inp["z"].view(np.int16)).view(bf).pin_memory(),
-                "slot": torch.from_numpy(ids).pin_memory(),
-            }
+            host_np.append({"xbc": (inp["xbc"].view(np.int16), bf), "dt": (inp["dt"], torch.float32),
+                            "z": (inp["z"].view(np.int16), bf), "slot": (ids, torch.int32)})
+        fields = list(host_np[0])
+        nbytes = {k: host_np[0][k][0].nbytes for k in fields}
+        self.layer_bytes = sum((nbytes[k] + 255) // 256 * 256 for k in fields)
+        self.host_flat = torch.empty(layers * self.layer_bytes, dtype=torch.uint8, pin_memory=True)
+        self.dev_flat = torch.empty(layers * self.layer_bytes, dtype=torch.uint8, device=dev)
+        for l in range(layers):
+            off = l * self.layer_bytes
+            host, devv = {}, {}
+            for k in fields:
+                arr, dtype = host_np[l][k]
+                nb = nbytes[k]
+                self.host_flat[off:off + nb].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+                host[k] = self.host_flat[off:off + nb].view(dtype).view(arr.shape)
+                devv[k] = self.dev_flat[off:off + nb].view(dtype).view(arr.shape)
+                off += (nb + 255) // 256 * 256
             self.host_inp.append(host)
-            self.inp.append({k: v.to(dev) for k, v in host.items() if k != "slot"})
+            self.slot.append(devv.pop("slot"))
+            self.inp.append(devv)
+        self.dev_flat.copy_(self.host_flat)
         self.y = torch.empty(layers, batch, 1, H * P, dtype=bf, device=dev)
         self.y_host = torch.empty(layers, batch, 1, H * P, dtype=bf).pin_memory()
         self.launches_per_step = layers
         # end-to-end pipeline: uploads on one stream, downloads on another, the launches on the
-        # caller's stream; events order each layer's buffers across streams and steps
+        # caller's stream; events order each group of layers' buffers across streams and steps
         self.s_up, self.s_down = torch.cuda.Stream(), torch.cuda.Stream()
-        ev = lambda: [torch.cuda.Event() for _ in range(layers)]
-        self.ev_in, self.ev_used, self.ev_y, self.ev_out = ev(), ev(), ev(), ev()
+        self.groups = e2e_groups(layers)
+        ev = lambda: [torch.cuda.Event() for _ in self.groups]
+        self.ev_in, self.ev_used, self.ev_out = ev(), ev(), ev()
+        self.ev_start = torch.cuda.Event()
 
     def step(self, stream=None):
         bd = self.bd
@@ -215,33 +242,45 @@ class DecodeWorkload:
 
     def step_e2e(self):
         """Host buffers in, result out: every layer's inputs copied from pinned memory, the 48
-        launches, and every layer's y copied back.  Layer l+1's upload runs while layer l computes
-        and layer l's y is downloaded while layer l+1 computes (three streams, per-layer events)."""
+        launches, and every layer's y copied back, all inside the step.  Layers go in groups
+        (`e2e_groups`): group g+1's upload runs while group g computes and group g's y is
+        downloaded while group g+1 computes (three streams, one event per group and stream).  The
+        launches inside a group follow each other with no stream dependency between them, so each
+        starts as the previous one completes (programmatic dependent launch); a group boundary
+        waits on that group's upload.  Only the first group's upload and the last group's download
+        (one layer each) are not overlapped with compute.  No upload starts before the previous
+        step has ended with its result on the host, as in a decode loop whose next inputs come
+        from the previous step's outputs."""
         torch, bd = self.torch, self.bd
         cur = torch.cuda.current_stream()
-        for l in range(self.layers):
-            h, d = self.host_inp[l], self.inp[l]
+        self.ev_start.record(cur)  # after the previous step's final wait: its y is on the host
+        l0 = 0
+        for gi, n in enumerate(self.groups):
+            layers = range(l0, l0 + n)
             with torch.cuda.stream(self.s_up):
-                self.s_up.wait_event(self.ev_used[l])  # the previous step's layer l has read its inputs
-                for k in ("xbc", "dt", "z"):
-                    d[k].copy_(h[k], non_blocking=True)
-                self.slot[l].copy_(h["slot"], non_blocking=True)
-                self.ev_in[l].record(self.s_up)
-            cur.wait_event(self.ev_in[l])
-            cur.wait_event(self.ev_out[l])  # the previous step's y of layer l has been downloaded
-            prm = self.prm[l]
-            bd.mamba_state_update(self.desc, self.ssm[l], self.slot[l], d["xbc"], d["dt"], prm["A"], self.y[l],
-                                  conv_pool=self.conv[l], conv_w=prm["conv_w"], D=prm["D"], dt_bias=prm["dt_bias"],
-                                  z=d["z"])
-            self.ev_used[l].record(cur)
+                if gi == 0:
+                    self.s_up.wait_event(self.ev_start)
+                self.s_up.wait_event(self.ev_used[gi])  # the previous step's group has read its inputs
+                a, b = l0 * self.layer_bytes, (l0 + n) * self.layer_bytes
+                self.dev_flat[a:b].copy_(self.host_flat[a:b], non_blocking=True)
+                self.ev_in[gi].record(self.s_up)
+            cur.wait_event(self.ev_in[gi])
+            cur.wait_event(self.ev_out[gi])  # the previous step's y of the group has been downloaded
+            for l in layers:
+                d, prm = self.inp[l], self.prm[l]
+                bd.mamba_state_update(self.desc, self.ssm[l], self.slot[l], d["xbc"], d["dt"], prm["A"], self.y[l],
+                                      conv_pool=self.conv[l], conv_w=prm["conv_w"], D=prm["D"],
+                                      dt_bias=prm["dt_bias"], z=d["z"])
+            self.ev_used[gi].record(cur)
             with torch.cuda.stream(self.s_down):
-                self.s_down.wait_event(self.ev_used[l])
-                self.y_host[l].copy_(self.y[l], non_blocking=True)
-                self.ev_out[l].record(self.s_down)
-        cur.wait_event(self.ev_out[self.layers - 1])  # the step ends when the last y is on the host
+                self.s_down.wait_event(self.ev_used[gi])
+                self.y_host[l0:l0 + n].copy_(self.y[l0:l0 + n], non_blocking=True)
+                self.ev_out[gi].record(self.s_down)
+            l0 += n
+        cur.wait_event(self.ev_out[-1])  # the step ends when the last y is on the host
 
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for h in self.host_inp for t in h.values())
+        return self.host_flat.numel()  # the inputs plus at most 255 bytes of padding per field
 
     def d2h_bytes(self):
         return self.y_host.numel() * self.y_host.element_size()

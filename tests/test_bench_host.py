@@ -121,3 +121,13 @@ def test_gpus_flag_must_match_the_launched_ranks():
                        capture_output=True, text=True, env=env, timeout=120)
     assert r.returncode != 0
     assert "WORLD_SIZE=1" in r.stderr and "torch.distributed.run" in r.stderr
+
+
+@pytest.mark.parametrize("layers", [1, 5, 21, 22, 48, 64])
+def test_e2e_groups_cover_every_layer_once(layers):
+    """The end-to-end pipeline's layer groups add up to the layer count, and the first and last
+    groups (whose upload and download are not hidden behind compute) hold one layer each."""
+    g = bench.e2e_groups(layers)
+    assert sum(g) == layers and min(g) >= 1
+    assert g[0] == 1 and g[-1] == 1
+    assert max(g) <= 8
