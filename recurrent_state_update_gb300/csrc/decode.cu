@@ -1290,7 +1290,7 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 // host side
 // ---------------------------------------------------------------------------------------
 
-// Persistent single-token launch: as many stages as fit beside the item buffers, one CTA per SM.
+// Persistent single-token launch, one CTA per SM, its ring depth chosen in launch_stream.
 // Returns 1 when the layer's conv / xBC / z segments are not 16-byte aligned for bulk copies (the
 // caller then uses the per-item kernel).
 // Whether a cluster of the configuration's size can be resident, remembered per (device, kernel,
@@ -1384,20 +1384,30 @@ static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     // could wait on a stage whose previous phase belongs to the other slot and is still pending,
     // and a parity wait cannot tell the two phases apart.  So ns is a multiple of NHS when NHS
     // divides HG, and a multiple of HG otherwise.
+    //
+    // Depth: at least two tiles in flight per head slot and 64 KB per CTA, or 128 KB when the
+    // launch gives each CTA fewer than six items (its first copies are then a large share), no
+    // more.  Measured on GB300 at the Nemotron shape, bf16 16 KB tiles, µs per launch at 4 / 6 / 8
+    // stages: batch 40 (2.1 items a CTA) 38.6 / 37.2 / 36.2, batch 96 (5.1) 74.6 / 72.1 / 71.9,
+    // batch 128 (6.7) 91.9 / 95.7 / 96.6, batch 256 (13.5) 178.2 / 179.6 / 182.1; fp32 32 KB tiles
+    // at batch 256: 340 µs at 2 stages, 347 at 4.  One tile per slot starves the stream.
+    const int sm_count = device_sms();
+    if (sm_count <= 0) return MAMBA_ECUDA;
+    const int W = a.batch * a.G;
+    const int grid = W < sm_count ? W : sm_count;
     constexpr int NHS = kStreamConsumers / Tile<StateT, P, N>::TH;
     const int step = (a.HG % NHS == 0) ? NHS : a.HG;
-    int ns = 16 - 16 % step;
-    while (ns > step && StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total > 220 * 1024) ns -= step;
+    const size_t want = (W < 6 * grid ? 128 : 64) * (size_t)1024;
+    int ns = step;
+    while (ns < 2 * NHS || (size_t)ns * tile < want) ns += step;
+    while (ns > step && (ns > 16 || StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total > 220 * 1024))
+        ns -= step;
     if (ns < step || ns % step != 0) return 1;
     const size_t smem = StreamSmem(ns, tile, LC, a.HG, P, a.W, a.Wc, es, dt_es).total;
     if (smem > 227 * 1024) return 1;
-    const int sm_count = device_sms();
-    if (sm_count <= 0) return MAMBA_ECUDA;
     StreamArgs sa;
     sa.d = a;
     sa.ns = ns;
-    const int W = a.batch * a.G;
-    const int grid = W < sm_count ? W : sm_count;
     auto kern = k_decode_stream<StateT, ActT, P, N>;
     if (!smem_limit(reinterpret_cast<const void *>(kern), smem)) return MAMBA_ECUDA;
     if (launch_pdl(kern, dim3(grid), dim3(kStreamThreads), smem, stream, sa) != cudaSuccess) return MAMBA_ECUDA;

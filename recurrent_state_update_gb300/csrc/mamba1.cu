@@ -351,7 +351,11 @@ bool launch_m1_stream(const M1Args &a, int batch, cudaStream_t st) {
         return false;
     const M1Stage L(N, (uint32_t)es, (uint32_t)ea);
     const size_t tail = 16 * 8 * 2 + 16;  // barriers of up to 16 stages + flags
-    int ns = 16;
+    // About 64 KB of stages per CTA (two CTAs per SM): deeper rings make each launch a little
+    // faster alone but the 64-layer conv + update step slower on GB300 (Mamba-2.8B-like shape,
+    // batch 256: 1.725 ms per step at 6 stages of 10.2 KB, 1.745 at 8, 1.794 at 10; 1.735 at 4).
+    int ns = 2;
+    while (ns < 16 && (size_t)(ns + 1) * L.bytes <= 64 * 1024) ++ns;
     while (ns > 2 && (size_t)ns * L.bytes + tail > 110 * 1024) --ns;
     const size_t smem = (size_t)ns * L.bytes + (size_t)ns * 16 + 16;
     const int sms = std::max(1, sm_count_m1());
