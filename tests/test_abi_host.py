@@ -302,3 +302,26 @@ def test_binding_rejects_tensors_of_the_wrong_dtype():
                             torch.zeros(1, 4, 16, dtype=bf), torch.zeros(1, 4, dtype=f32), ok["A"],
                             torch.zeros(1, 1, 16, dtype=bf), torch.zeros(1, 1, 16, dtype=bf),
                             torch.zeros(1, 4, 16, dtype=bf), None, has_initial_state=torch.zeros(1, dtype=torch.bool))
+
+
+def test_zero_size_calls_launch_nothing(lib):
+    """A call with no rows (or no sequences) returns MAMBA_OK before touching any pointer or the
+    device: the Mamba1 step and conv, the speculative commit and the allocation-free prefill
+    (the other entry points' zero-size calls are checked with their argument errors above)."""
+    d = bd.layer_desc(wl.NEMOTRON_H_8B)
+    d1 = bd.mamba1_desc(5120, 16)
+    assert lib.mamba1_state_update(ctypes.byref(d1), None, 5120 * 16, 8, None, 0, None, None, None, None, None,
+                                   None, None, 1, None, None, None, None) == bd.MAMBA_OK
+    assert lib.mamba1_conv_update(ctypes.byref(d1), None, 5120 * 3, 8, None, 0, 1, None, None, None, None, None,
+                                  None) == bd.MAMBA_OK
+    assert lib.mamba_spec_commit(ctypes.byref(d), None, 128 * 64 * 128, 8, None, 0, None, None, None, 0, 4, None,
+                                 None) == bd.MAMBA_OK
+    assert lib.mamba_chunk_scan_noalloc(ctypes.byref(d), None, 128 * 64 * 128, 8, None, 0, 0, None, None, None, 0,
+                                        0, 256, None, None, None, None, None, None, None, 1, None, None, None,
+                                        None) == bd.MAMBA_OK
+    # negative sizes are argument errors, not empty calls
+    assert lib.mamba1_state_update(ctypes.byref(d1), None, 5120 * 16, 8, None, -1, None, None, None, None, None,
+                                   None, None, 1, None, None, None, None) == bd.MAMBA_EINVAL
+    assert lib.mamba_chunk_scan_noalloc(ctypes.byref(d), None, 128 * 64 * 128, 8, None, -1, 0, None, None, None, 0,
+                                        0, 256, None, None, None, None, None, None, None, 1, None, None, None,
+                                        None) == bd.MAMBA_EINVAL
