@@ -1,4 +1,4 @@
-"""GPU parity in the method's degenerate case and with the step passed raw.
+"""GPU parity in the method's degenerate case, with the step passed raw, and with the conv bias.
 
 * A zero step: dt = 0 with softplus off and no dt_bias makes Delta = 0, so exp(Delta A) = 1 and
   Delta x B^T = 0 and the recurrence leaves the state as it was (echobase "Mamba" notes, the
@@ -7,6 +7,7 @@
   slot's state), while y is C.h + D.x of that state and the conv windows still shift.
 * Raw steps: with softplus off the step is dt + dt_bias itself ("Hybrid SSM / Mamba models and
   non-KV state", the decode call's `dt_softplus` flag); against the oracle with softplus off.
+* The conv's optional bias on every decode launch path and in the standalone conv update.
 
 Tolerances as in the other parity tests: bf16 per-tile max error 2e-2, fp32 1e-4 (prefill) and
 1e-5 (Mamba1), conv windows bit-exact.
@@ -184,3 +185,78 @@ def test_mamba1_with_softplus_off(zero):
             np.testing.assert_array_equal(after[s], wl.upcast(pool0[s], wl.BF16))
         else:
             assert tile_rel_err(after[s], h, 2) < 2e-2
+
+
+# (batch, ntok) as above, plus the standalone conv update (one token: the 16-byte single-token
+# kernel; three tokens: the general one)
+@pytest.mark.parametrize("batch,ntok", DECODE_PATHS)
+def test_decode_with_conv_bias(batch, ntok):
+    """The conv's optional bias (the pages' conv has one; the workloads pass none) on every decode
+    launch path, against the oracle: outputs, states and the windows (bit-exact)."""
+    import torch
+    shape = wl.NEMOTRON_H_8B.with_spec(ntok if ntok > 1 else 0)
+    H, P, Cd = shape.nheads, shape.head_dim, shape.conv_dim
+    seed = 200 + batch + ntok
+    g = wl.rng(seed, 0)
+    prm = wl.layer_params(g, shape)
+    bias = wl.store(g.standard_normal(Cd) / 4, wl.F32)
+    S = batch * (1 + (ntok if ntok > 1 else 0)) + 8
+    st = wl.initial_states(wl.rng(seed, 1), shape, S, wl.BF16, wl.BF16)
+    ids = wl.rng(seed, 2).permutation(S).astype(np.int32)
+    slot = ids[:batch]
+    scratch = ids[batch:batch + batch * ntok].reshape(batch, ntok) if ntok > 1 else None
+    inp = wl.decode_inputs(wl.rng(seed, 3), shape, prm, batch, ntok, wl.BF16)
+    g_ssm, g_conv = guarded(to_dev(st["ssm"], wl.BF16)), guarded(to_dev(st["conv"], wl.BF16))
+    ssm, conv = g_ssm.t, g_conv.t
+    g_y = guarded(torch.empty(batch, ntok, H * P, dtype=torch.bfloat16, device="cuda"))
+    d = {k: to_dev(v, wl.F32) for k, v in prm.items()}
+    bd.mamba_state_update(bd.layer_desc(shape), ssm, to_i32(slot), to_dev(inp["xbc"], wl.BF16),
+                          to_dev(inp["dt"], wl.F32), d["A"], g_y.t, conv_pool=conv, conv_w=d["conv_w"],
+                          conv_b=to_dev(bias, wl.F32), scratch_slots=None if scratch is None else to_i32(scratch),
+                          D=d["D"], dt_bias=d["dt_bias"], z=to_dev(inp["z"], wl.BF16))
+    torch.cuda.synchronize()
+    for g_, what in ((g_ssm, "the state pool"), (g_conv, "the conv pool"), (g_y, "y")):
+        g_.check(what)
+    o_ssm, o_conv = wl.upcast(st["ssm"], wl.BF16), wl.upcast(st["conv"], wl.BF16)
+    y_o = oracle.decode(o_ssm, slot, wl.upcast(inp["xbc"], wl.BF16), inp["dt"].astype(np.float64),
+                        prm["A"].astype(np.float64), conv_pool=o_conv, conv_w=prm["conv_w"].astype(np.float64),
+                        conv_b=wl.upcast(bias, wl.F32), scratch=scratch, D=prm["D"].astype(np.float64),
+                        dt_bias=prm["dt_bias"].astype(np.float64),
+                        z=wl.upcast(inp["z"], wl.BF16).reshape(batch, ntok, H, P), n_groups=shape.n_groups)
+    got_y = f64(g_y.t)
+    assert tile_rel_err(got_y.reshape(batch, ntok, H, -1), y_o.reshape(batch, ntok, H, -1), 1) < 2e-2
+    np.testing.assert_array_equal(f64(conv[torch.from_numpy(slot).long().cuda()]), o_conv[slot])
+    for tg in ([slot] if scratch is None else [scratch[:, j] for j in range(ntok)]):
+        assert tile_rel_err(f64(ssm[torch.from_numpy(tg.copy()).long().cuda()]), o_ssm[tg], 2) < 2e-2
+
+
+@pytest.mark.parametrize("ntok", [1, 3])
+def test_conv_update_with_bias(ntok):
+    """The standalone conv update with a bias: outputs within 2^-8 of the tile maximum, windows
+    bit-exact, padded rows untouched."""
+    import torch
+    S, batch, seed = 24, 10, 210 + ntok
+    shape = wl.NEMOTRON_H_8B.with_spec(2)
+    Cd = shape.conv_dim
+    g = wl.rng(seed, 0)
+    prm = wl.layer_params(g, shape)
+    bias = wl.store(g.standard_normal(Cd) / 4, wl.F32)
+    st = wl.initial_states(wl.rng(seed, 1), shape, S, wl.BF16, wl.BF16)
+    slot = wl.slot_ids(wl.rng(seed, 2), S, batch, 0.2)
+    inp = wl.decode_inputs(wl.rng(seed, 3), shape, prm, batch, ntok, wl.BF16)
+    conv = to_dev(st["conv"], wl.BF16)
+    out = torch.zeros(batch, ntok, Cd, device="cuda", dtype=torch.bfloat16)
+    bd.mamba_conv_update(bd.layer_desc(shape), conv, to_i32(slot), to_dev(inp["xbc"], wl.BF16),
+                         to_dev(prm["conv_w"], wl.F32), out, conv_b=to_dev(bias, wl.F32))
+    torch.cuda.synchronize()
+    got, o_conv = f64(conv), wl.upcast(st["conv"], wl.BF16)
+    for i, s in enumerate(slot):
+        if s < 0:
+            assert bool((out[i] == 0).all())
+            continue
+        new, ref = oracle.conv_update(o_conv[s], wl.upcast(inp["xbc"], wl.BF16)[i],
+                                      prm["conv_w"].astype(np.float64), wl.upcast(bias, wl.F32))
+        np.testing.assert_array_equal(got[s], new)
+        assert np.abs(f64(out[i]) - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-6
+    dead = np.setdiff1d(np.arange(S), slot)
+    np.testing.assert_array_equal(got[dead], o_conv[dead])
