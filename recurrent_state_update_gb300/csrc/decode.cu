@@ -1269,7 +1269,22 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
                                                             (int64_t)src * a.ssm_stride + unit * tile_bytes);
         uint4 *to = reinterpret_cast<uint4 *>(static_cast<char *>(a.ssm_pool) + (int64_t)s * a.ssm_stride +
                                               unit * tile_bytes);
-        for (int v = tid; v < a.tile_vecs; v += blockDim.x) __stcs(to + v, __ldcs(from + v));
+        // every load of a batch is issued before its stores (source and destination may alias as far
+        // as the compiler knows, so a plain copy loop would keep one load in flight per thread)
+        constexpr int kBatch = 4;
+        for (int v0 = tid; v0 < a.tile_vecs; v0 += blockDim.x * kBatch) {
+            uint4 r[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int v = v0 + q * (int)blockDim.x;
+                if (v < a.tile_vecs) r[q] = __ldcs(from + v);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int v = v0 + q * (int)blockDim.x;
+                if (v < a.tile_vecs) __stcs(to + v, r[q]);
+            }
+        }
         return;
     }
     if (!a.conv_pool) return;
@@ -1290,9 +1305,6 @@ __global__ void __launch_bounds__(256) k_spec_commit(const CommitArgs a) {
 // host side
 // ---------------------------------------------------------------------------------------
 
-// Persistent single-token launch, one CTA per SM, its ring depth chosen in launch_stream.
-// Returns 1 when the layer's conv / xBC / z segments are not 16-byte aligned for bulk copies (the
-// caller then uses the per-item kernel).
 // Whether a cluster of the configuration's size can be resident, remembered per (device, kernel,
 // cluster size, block, shared memory) so that small-batch calls do not repeat the occupancy query.
 static bool cluster_fits(const void *kern, const cudaLaunchConfig_t &cfg) {
@@ -1364,6 +1376,9 @@ static int device_sms() {
     return n;
 }
 
+// Persistent single-token launch, one CTA per SM, its ring depth chosen below.  Returns 1 when the
+// layer's conv / xBC / z segments are not 16-byte aligned for bulk copies (the caller then uses
+// the per-item kernel).
 template <typename StateT, typename ActT, int P, int N>
 static int launch_stream(const DecodeArgs &a, cudaStream_t stream) {
     const int LC = a.HG * P + 2 * N;
