@@ -1449,8 +1449,14 @@ static int launch_decode_shape(const DecodeArgs &a0, int ntok, int P_, int N_, c
     // Small single-token batches: batch x groups CTAs would leave most SMs idle, so the heads of a
     // group are split over a cluster of up to 8 CTAs (a power of two dividing the heads per group,
     // at most enough for two CTAs per SM).
+    //
+    // Several tokens at batches that already fill the GPU: two CTAs per group (8 heads each at the
+    // Nemotron shape) make the launch's last partial wave shorter.  Batch 128, 4 drafts on GB300:
+    // 0.307 ms per draft + commit step against 0.312 unsplit and 0.344 with four CTAs per group.
     int ksplit = 1;
     const int sms = device_sms();
+    if (vec && ntok > 1 && sms > 0 && (int64_t)a.batch * a.G >= 2 * sms && a.HG % 2 == 0 && ((a.HG / 2) * P) % VA == 0)
+        ksplit = 2;
     if (vec && ntok == 1 && sms > 0 && (int64_t)a.batch * a.G < 2 * sms) {
         const int64_t want = (2 * (int64_t)sms + (int64_t)a.batch * a.G - 1) / ((int64_t)a.batch * a.G);
         while (ksplit * 2 <= 8 && ksplit * 2 <= want && a.HG % (ksplit * 2) == 0 && ((a.HG / (ksplit * 2)) * P) % VA == 0)

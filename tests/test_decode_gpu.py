@@ -546,6 +546,7 @@ OTHER_TILES = [
     (128, 128, 4, 1, 4, wl.BF16, wl.BF16, 320, 1, 0),
     (128, 128, 4, 2, 3, wl.F32, wl.F32, 5, 2, 2),
     (32, 64, 8, 2, 4, wl.BF16, wl.BF16, 40, 3, 3),
+    (32, 64, 8, 2, 4, wl.BF16, wl.BF16, 160, 2, 2),  # several tokens, two CTAs per group
     (64, 128, 16, 2, 4, wl.BF16, wl.F32, 50, 1, 0),
     (16, 16, 4, 1, 4, wl.BF16, wl.BF16, 400, 1, 0),
 ]
