@@ -1152,7 +1152,7 @@ __global__ void __launch_bounds__(kConvThreads) k_conv_step(const ConvArgs a, in
             float acc = fmaf(wv[v * W + W - 1], x[v], bv[v]);
 #pragma unroll
             for (int c = 0; c < W - 1; ++c) acc = fmaf(wv[v * W + c], cur[v * (W - 1) + c], acc);
-            o[v] = silu_f(acc);
+            o[v] = silu_fast(acc);
         }
         *reinterpret_cast<uint4 *>(static_cast<ActT *>(a.xbc_out) + (int64_t)(i0 + r) * a.Cd + c0) = pack16(o);
         // new window: every channel's columns shifted left by one, the token appended
