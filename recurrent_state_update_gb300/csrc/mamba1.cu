@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kM1Threads, N <= 16 ? 3 : 1) k_mamba1_update(c
 // channels' rows of A, D and dt_bias stay in registers) and walks the rows rb, rb + kpb, ...
 // One producer thread bulk-copies each item's state rows (kM1Threads x N contiguous values in the
 // slot), x, dt and z slices and the row's B and C into a ring of shared-memory stages, up to NS
-// items ahead; 256 consumer threads (one channel each) update the state from the stage, write it
+// items ahead (three CTAs per SM); 256 consumer threads (one channel each) update the state from the stage, write it
 // back with evict-first 16-byte stores and write y.  Each stage has a full barrier (the copies'
 // bytes) and an empty barrier (every consumer has used the stage).  All waits are bounded.
 
@@ -190,7 +190,7 @@ __device__ __forceinline__ float act_at(const unsigned char *p, int t) {
 }
 
 template <typename StateT, typename ActT, int N>
-__global__ void __launch_bounds__(kM1StreamThreads, 2) k_mamba1_stream(const M1StreamArgs sa) {
+__global__ void __launch_bounds__(kM1StreamThreads, 3) k_mamba1_stream(const M1StreamArgs sa) {
     pdl_wait();
     pdl_launch_dependents();
     const M1Args &a = sa.a;
@@ -351,16 +351,16 @@ bool launch_m1_stream(const M1Args &a, int batch, cudaStream_t st) {
         return false;
     const M1Stage L(N, (uint32_t)es, (uint32_t)ea);
     const size_t tail = 16 * 8 * 2 + 16;  // barriers of up to 16 stages + flags
-    // About 64 KB of stages per CTA (two CTAs per SM): deeper rings make each launch a little
-    // faster alone but the 64-layer conv + update step slower on GB300 (Mamba-2.8B-like shape,
-    // batch 256: 1.725 ms per step at 6 stages of 10.2 KB, 1.745 at 8, 1.794 at 10; 1.735 at 4).
+    // Three CTAs per SM with about 40 KB of stages each.  GB300, Mamba-2.8B-like shape, batch 256,
+    // 64-layer conv + update step: 1.648 ms at 4 stages of 10.2 KB, 1.652 at 3, 1.661 at 6.  Two
+    // CTAs per SM took 1.70 ms at their best depth (6 stages; 10 stages 1.79 ms).
     int ns = 2;
-    while (ns < 16 && (size_t)(ns + 1) * L.bytes <= 64 * 1024) ++ns;
-    while (ns > 2 && (size_t)ns * L.bytes + tail > 110 * 1024) --ns;
+    while (ns < 16 && (size_t)(ns + 1) * L.bytes <= 42 * 1024) ++ns;
+    while (ns > 2 && (size_t)ns * L.bytes + tail > 72 * 1024) --ns;
     const size_t smem = (size_t)ns * L.bytes + (size_t)ns * 16 + 16;
     const int sms = std::max(1, sm_count_m1());
     const int ncb = (a.Dn + kM1Threads - 1) / kM1Threads;
-    const int kpb = std::min(batch, std::max(1, 2 * sms / ncb));
+    const int kpb = std::min(batch, std::max(1, 3 * sms / ncb));
     auto kern = k_mamba1_stream<StateT, ActT, N>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
     M1StreamArgs sa;
