@@ -192,7 +192,7 @@ class DecodeWorkload:
             self.conv[l].copy_(torch.randn(pool, CD, W1, generator=gen, device=dev).mul_(0.1))
         # Every layer's step inputs (xbc, dt, z, slot ids) packed back to back in one pinned host
         # buffer and its device copy, so that the inputs of a run of layers move in one copy.
-        self.prm, self.slot, self.inp, self.host_inp = [], [], [], []
+        self.prm, self.slot, self.inp = [], [], []
         host_np = []
         for l in range(layers):
             g = wl.rng(seed, l)
@@ -209,15 +209,13 @@ class DecodeWorkload:
         self.dev_flat = torch.empty(layers * self.layer_bytes, dtype=torch.uint8, device=dev)
         for l in range(layers):
             off = l * self.layer_bytes
-            host, devv = {}, {}
+            devv = {}
             for k in fields:
                 arr, dtype = host_np[l][k]
                 nb = nbytes[k]
                 self.host_flat[off:off + nb].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
-                host[k] = self.host_flat[off:off + nb].view(dtype).view(arr.shape)
                 devv[k] = self.dev_flat[off:off + nb].view(dtype).view(arr.shape)
                 off += (nb + 255) // 256 * 256
-            self.host_inp.append(host)
             self.slot.append(devv.pop("slot"))
             self.inp.append(devv)
         self.dev_flat.copy_(self.host_flat)
