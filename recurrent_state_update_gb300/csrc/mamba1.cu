@@ -156,9 +156,10 @@ __global__ void __launch_bounds__(kM1Threads, N <= 16 ? 3 : 1) k_mamba1_update(c
 // channels' rows of A, D and dt_bias stay in registers) and walks the rows rb, rb + kpb, ...
 // One producer thread bulk-copies each item's state rows (kM1Threads x N contiguous values in the
 // slot), x, dt and z slices and the row's B and C into a ring of shared-memory stages, up to NS
-// items ahead (three CTAs per SM); 256 consumer threads (one channel each) update the state from the stage, write it
-// back with evict-first 16-byte stores and write y.  Each stage has a full barrier (the copies'
-// bytes) and an empty barrier (every consumer has used the stage).  All waits are bounded.
+// items ahead; 256 consumer threads (one channel each) update the state from the stage, write it
+// back with evict-first 16-byte stores and write y.  Three CTAs share an SM.  Each stage has a
+// full barrier (the copies' bytes) and an empty barrier (every consumer has used the stage).
+// All waits are bounded.
 
 constexpr int kM1StreamThreads = kM1Threads + 32;
 constexpr uint32_t kM1Polls = umma::kWaitPolls;
