@@ -489,7 +489,7 @@ def run_gpu(args):
     # end to end: pinned host inputs in, every layer's y out, inside the timed region
     e2e = None
     if args.only in ("all", "decode"):
-        ms_e2e = _max_over_ranks(torch, dist, _time(torch, dec.step_e2e, args.steps, 2, dist))
+        ms_e2e = _max_over_ranks(torch, dist, _time(torch, dec.step_e2e, args.steps, max(args.warmup, 3), dist))
         e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
     del dec
